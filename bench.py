@@ -1,0 +1,560 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged GQA attention path on GB300.
+
+Headline (one JSON line on stdout): a decode step of the decode-attention
+workload -- batch 64, Qwen3-0.6B attention shapes (16 query heads, 8 KV heads,
+head_dim 128, bf16), 256-token blocks, context lengths uniform in
+[512, 4096], physical blocks a random permutation of a pool 1.25x the blocks
+used.  One step = slot mapping + KV scatter of the new token + decode
+attention (split-K + combine), all through the C ABI.  value = KV bytes the
+attention reads per step / step time, in GB/s.
+
+The same line carries:
+  roofline      the decode attention call's achieved HBM GB/s (KV bytes per
+                call / CUDA-event time of the call) against the measured copy
+                bandwidth, plus DRAM traffic per launch from the committed ncu
+                summary when the kernel source is unchanged since it was taken
+  e2e           the same metric with host buffers: pinned-host -> device copies
+                of the step's inputs and the device -> host copy of its output
+                inside the timed region
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  secondary     prefill TFLOP/s (32 prompts with prefix-cache hits), long-
+                context decode GB/s (batch 8, 16k-40k), and the full 28-layer
+                decode step + sampler (batch 256) in tokens/s
+  clocks        SM clocks and throttle reasons sampled during the timed region
+
+``--impl reference`` times the CPU oracle instead (the only other arm: the
+pages ship no code to run), on the same metric and workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn HBM GB/s (% of peak); prefill TFLOP/s; decode tok/s at batch"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+DECODE_SRC = os.path.join(ROOT, "paged_kv_attention_29_gb300", "csrc", "decode.cu")
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file, src_path):
+    """DRAM bytes per launch from a committed ncu summary, if the source is unchanged."""
+    try:
+        with open(os.path.join(PROFILE_DIR, kernel_file)) as f:
+            rec = json.load(f)
+        if rec.get("source_sha256_16") == source_hash(src_path):
+            return rec.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0, interval_ms=50):
+        self.proc = None
+        self.t0 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t0 = time.time()
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), sm_max=float(parts[2]), reasons=parts[4:9]))
+            except ValueError:
+                continue
+        return rows
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names[1:], r["reasons"][1:]):
+                if v.lower() in ("active", "1", "true"):
+                    reasons.add(n)
+        loaded = [r["sm"] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r["sm_max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and --impl reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_decode_sample(wl, k_cache, v_cache, q, k_new, v_new, rows):
+    """The oracle's decode step (scatter + attention) for the given sequences,
+    on a compact pool that holds only their blocks.  Returns KV bytes covered."""
+    from oracle import paged_attention as pa
+    ids = sorted({int(x) for r in rows for x in wl.block_tables[r] if x >= 0})
+    remap = {b: i for i, b in enumerate(ids)}
+    kc = k_cache[ids]
+    vc = v_cache[ids]
+    bt = np.full((len(rows), wl.block_tables.shape[1]), -1, dtype=np.int64)
+    for i, r in enumerate(rows):
+        for j, x in enumerate(wl.block_tables[r]):
+            if x >= 0:
+                bt[i, j] = remap[int(x)]
+    lens = wl.kv_lens[rows]
+    slots = pa.slot_mapping(np.ones(len(rows), np.int64), lens, bt, wl.block_size)
+    kc, vc = pa.store_kvcache(kc, vc, k_new[rows], v_new[rows], slots, wl.block_size)
+    pa.decode(q[rows], kc, vc, bt, lens, wl.block_size, wl.softmax_scale)
+    return int(lens.astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * 2
+
+
+def cpu_inputs(wl, device_vals=None):
+    """Float32 CPU copies of the workload's values (exact for bf16)."""
+    if device_vals is None:
+        device_vals = W.paged_values(wl, device="cpu")
+    f = lambda t: t.detach().to("cpu").float().numpy()  # noqa: E731
+    return (f(device_vals.k_cache), f(device_vals.v_cache), f(device_vals.q), f(device_vals.k_new),
+            f(device_vals.v_new))
+
+
+def time_oracle(wl, arrays, budget_s, min_rows=1):
+    """Run oracle decode steps on growing prefixes of the batch until ~budget_s."""
+    kc, vc, q, kn, vn = arrays
+    t0 = time.perf_counter()
+    bytes_done = 0
+    rows_done = 0
+    r = 0
+    while True:
+        rows = [r % wl.batch]
+        bytes_done += oracle_decode_sample(wl, kc, vc, q, kn, vn, rows)
+        rows_done += 1
+        r += 1
+        if time.perf_counter() - t0 >= budget_s and rows_done >= min_rows:
+            break
+    dt = time.perf_counter() - t0
+    return bytes_done / dt / 1e9, rows_done, dt
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = W.decode_b64()
+    arrays = cpu_inputs(wl)
+    # calibrate one sequence, then size each step so the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    oracle_decode_sample(wl, *arrays, rows=[0])
+    t_one = max(time.perf_counter() - t0, 1e-3)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    n_rows = int(min(wl.batch, max(1, per_step // t_one)))
+    kc, vc, q, kn, vn = arrays
+    for i in range(args.warmup):
+        oracle_decode_sample(wl, kc, vc, q, kn, vn, [(i * n_rows + j) % wl.batch for j in range(n_rows)])
+    tot_bytes = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        tot_bytes += oracle_decode_sample(wl, kc, vc, q, kn, vn, [(i * n_rows + j) % wl.batch for j in range(n_rows)])
+    dt = time.perf_counter() - t0
+    value = tot_bytes / dt / 1e9
+    threads = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS") or "1"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": decode_config_dict(wl),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": int(threads), "kind": "oracle",
+                         "sample": f"{n_rows} of {wl.batch} sequences per step (KV scatter + fp64 gather-then-dense "
+                                   f"attention), compact pool of their blocks"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def decode_config_dict(wl):
+    return {"workload": "decode attention, one layer: batch 64, Hq 16, Hkv 8, d 128, bf16, block 256, "
+                        "context U[512,4096], pool 1.25x blocks used, random block permutation",
+            "batch": wl.batch, "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
+            "head_dim": wl.head_dim, "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+            "kv_bytes_per_step": wl.kv_bytes_read, "seed": wl.seed,
+            "l2": f"inputs larger than L2 (KV {wl.kv_bytes_read / 1e9:.2f} GB per step vs 0.13 GB L2)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class DecodeStep:
+    """Device-resident decode workload and its step (slot map + scatter + decode)."""
+
+    def __init__(self, pkv, torch, wl, layers=1, seed_offset=0):
+        self.pkv, self.torch, self.wl = pkv, torch, wl
+        dev = "cuda"
+        self.layers = []
+        for layer in range(layers):
+            v = W.paged_values(wl, device=dev, layer=layer + seed_offset)
+            self.layers.append(v)
+        self.block_tables = torch.from_numpy(wl.block_tables).to(dev)
+        self.ctx = torch.from_numpy(wl.kv_lens).to(dev)
+        self.slots = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.layers[0].q)
+        self.ws = pkv.decode_workspace(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim)
+        self.max_ctx = int(wl.kv_lens.max())
+        self.ev = None
+
+    def layer(self, i, q=None, k_new=None, v_new=None, events=None):
+        v = self.layers[i]
+        pkv, wl = self.pkv, self.wl
+        pkv.pkv_slot_mapping(self.block_tables, wl.num_blocks, wl.block_size, self.slots, context_lens=self.ctx)
+        pkv.pkv_store_kvcache(k_new if k_new is not None else v.k_new, v_new if v_new is not None else v.v_new,
+                              self.slots, v.k_cache, v.v_cache)
+        if events is not None:
+            events[0].record()
+        pkv.pkv_decode(q if q is not None else v.q, v.k_cache, v.v_cache, self.block_tables, self.ctx, self.max_ctx,
+                       wl.softmax_scale, out=self.out, workspace=self.ws)
+        if events is not None:
+            events[1].record()
+        return self.out
+
+    LAUNCHES_PER_LAYER = 4   # slot mapping, scatter, split-K decode, combine
+
+
+def bench_headline(args, pkv, torch, dist, ws, rank, peaks):
+    wl = W.decode_b64()
+    step = DecodeStep(pkv, torch, wl)
+    cpu_arrays = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v = step.layers[0]
+        f = lambda t: t.detach().to("cpu").float().numpy()  # noqa: E731
+        cpu_arrays = (f(v.k_cache), f(v.v_cache), f(v.q), f(v.k_new), f(v.v_new))  # before any kernel runs
+    for _ in range(args.warmup):
+        step.layer(0)
+    torch.cuda.synchronize()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    time.sleep(0.2)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(K):
+        step.layer(0, events=evs[k])
+    end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clock_rows = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    call_ms = [a.elapsed_time(b) for a, b in evs]
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / K
+    value = wl.kv_bytes_read * ws / (ms_per_step * 1e-3) / 1e9
+    hbm, _, _, peak_kind = peaks
+    call_mean = float(np.mean(call_ms))
+    achieved = wl.kv_bytes_read / (call_mean * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": profiled_traffic("decode_splitk_b64_traffic.json", DECODE_SRC),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "kernel": "pkv_decode call (split-K decode + combine), CUDA events on the launching stream",
+                "algorithmic_bytes_per_launch": wl.kv_bytes_read}
+    e2e = bench_e2e(args, pkv, torch, step, dist, ws)
+    res = dict(value=value, ms_per_step=ms_per_step, roofline=roofline, e2e=e2e,
+               clocks=ClockSampler.summary(clock_rows), gpu_launches=K * DecodeStep.LAUNCHES_PER_LAYER,
+               config=decode_config_dict(wl), call_ms=call_mean)
+    return res, cpu_arrays, wl
+
+
+def bench_e2e(args, pkv, torch, step, dist, ws):
+    """Same step through the public API with host buffers and copies in the timed region."""
+    wl = step.wl
+    v = step.layers[0]
+    h_q = v.q.cpu().pin_memory()
+    h_k = v.k_new.cpu().pin_memory()
+    h_v = v.v_new.cpu().pin_memory()
+    h_bt = torch.from_numpy(wl.block_tables).pin_memory()
+    h_ctx = torch.from_numpy(wl.kv_lens).pin_memory()
+    h_out = torch.empty(tuple(v.q.shape), dtype=v.q.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(v.q), torch.empty_like(v.k_new), torch.empty_like(v.v_new)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+    K = max(10, args.steps // 4)
+
+    def one():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        step.block_tables.copy_(h_bt, non_blocking=True)
+        step.ctx.copy_(h_ctx, non_blocking=True)
+        out = step.layer(0, q=d_q, k_new=d_k, v_new=d_v)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(K):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / K
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": wl.kv_bytes_read * ws / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K}
+
+
+def flush_l2(torch, buf):
+    buf.add_(1)
+
+
+def bench_prefill(args, pkv, torch, peaks):
+    wl = W.prefill_prefix()
+    dev = "cuda"
+    v = W.paged_values(wl, device=dev)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    cu_q = torch.from_numpy(wl.cu_seqlens_q).to(dev)
+    cu_k = torch.from_numpy(wl.cu_seqlens_k).to(dev)
+    slots = torch.empty(wl.total_q, dtype=torch.int32, device=dev)
+    out = torch.empty_like(v.q)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    pairs = 0
+    for ql, kl in zip(wl.q_lens.astype(np.int64), wl.kv_lens.astype(np.int64)):
+        pairs += ql * (kl - ql) + ql * (ql + 1) // 2      # unmasked (query, key) pairs per head
+    flops = 4 * wl.head_dim * wl.num_heads * pairs
+
+    def step(evs=None):
+        pkv.pkv_slot_mapping(bt, wl.num_blocks, wl.block_size, slots, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
+        pkv.pkv_store_kvcache(v.k_new, v.v_new, slots, v.k_cache, v.v_cache)
+        if evs:
+            evs[0].record()
+        pkv.pkv_prefill_varlen(v.q, v.k_cache, v.v_cache, cu_q, cu_k, bt, int(wl.q_lens.max()),
+                               int(wl.kv_lens.max()), wl.softmax_scale, out=out)
+        if evs:
+            evs[1].record()
+
+    for _ in range(max(3, args.warmup // 10)):
+        step()
+    K = max(10, min(200, args.steps // 10))
+    step_ms, call_ms = [], []
+    for _ in range(K):
+        flush_l2(torch, flush)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        step((a, b))
+        e.record()
+        torch.cuda.synchronize()
+        step_ms.append(s.elapsed_time(e))
+        call_ms.append(a.elapsed_time(b))
+    _, bf16, bf16_sus, kind = peaks
+    call = float(np.median(call_ms))
+    tflops = flops / (call * 1e-3) / 1e12
+    return {"workload": "varlen prefill with prefix-cache hits: 32 prompts U[100,1024], 0-2 shared 256-token blocks "
+                        "per group of 4, Hq 16, Hkv 8, d 128, bf16",
+            "tflops": tflops, "unit": "TFLOP/s", "algorithmic_flops": int(flops), "call_ms_median": call,
+            "step_ms_median": float(np.median(step_ms)), "frac_of_bf16_peak": tflops / bf16,
+            "peak": bf16, "peak_source": kind, "steps": K, "l2": "flushed between steps (256 MB write)",
+            "total_q": wl.total_q}
+
+
+def bench_long_decode(args, pkv, torch, peaks):
+    wl = W.long_decode()
+    st = DecodeStep(pkv, torch, wl)
+    for _ in range(3):
+        st.layer(0)
+    K = max(10, min(200, args.steps // 10))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for k in range(K):
+        st.layer(0, events=evs[k])
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    gbs = wl.kv_bytes_read / (ms * 1e-3) / 1e9
+    res = {"workload": "long-context decode: batch 8, context U[16384,40960], pool 1400 blocks",
+           "gbs": gbs, "unit": "GB/s", "call_ms": ms, "frac_of_hbm": gbs / peaks[0], "kv_bytes": wl.kv_bytes_read}
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_full_step(args, pkv, torch, peaks):
+    wl = W.full_step()
+    st = DecodeStep(pkv, torch, wl, layers=wl.num_layers)
+    s_in = W.sampler_inputs(batch=wl.batch, device="cuda")
+    ids = torch.empty(wl.batch, dtype=torch.int64, device="cuda")
+
+    def step(k, evs=None):
+        for layer in range(wl.num_layers):
+            st.layer(layer)
+        if evs:
+            evs[0].record()
+        pkv.pkv_sample(s_in.logits, s_in.temperatures, s_in.seed + k, 0, out_ids=ids)
+        if evs:
+            evs[1].record()
+
+    for k in range(3):
+        step(k)
+    K = max(5, min(30, args.steps // 100))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    samp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    s.record()
+    for k in range(K):
+        step(k, samp[k])
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / K
+    sample_ms = float(np.mean([a.elapsed_time(b) for a, b in samp]))
+    kv = wl.kv_bytes_read * wl.num_layers
+    logits_bytes = wl.batch * W.VOCAB_QWEN3 * 4
+    res = {"workload": "full decode step: 28 layers x (slot map + scatter + decode), batch 256, context "
+                       "U[128,2048], per-layer pools, then the sampler on [256, 151936] fp32 logits",
+           "tok_per_s": wl.batch / (ms * 1e-3), "step_ms": ms, "kv_gbs": (kv + logits_bytes) / (ms * 1e-3) / 1e9,
+           "sampler_ms": sample_ms, "sampler_gbs": logits_bytes / (sample_ms * 1e-3) / 1e9,
+           "kv_bytes_per_step": kv, "steps": K,
+           "gpu_launches_per_step": wl.num_layers * DecodeStep.LAUNCHES_PER_LAYER + 1}
+    del st
+    torch.cuda.empty_cache()
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--no-secondary", action="store_true", help="headline only")
+    ap.add_argument("--parts", default="prefill,long,full",
+                    help="secondary workloads to run: any of prefill,long,full")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    import paged_kv_attention_29_gb300 as pkv
+    pkv.load()
+    peaks = load_peaks()
+
+    head, cpu_arrays, wl = bench_headline(args, pkv, torch, dist, ws, rank, peaks)
+    secondary = {}
+    parts = set() if args.no_secondary else {x.strip() for x in args.parts.split(",") if x.strip()}
+    if rank == 0:
+        if "prefill" in parts:
+            secondary["prefill"] = bench_prefill(args, pkv, torch, peaks)
+        if "long" in parts:
+            secondary["long_decode"] = bench_long_decode(args, pkv, torch, peaks)
+        if "full" in parts:
+            secondary["full_step"] = bench_full_step(args, pkv, torch, peaks)
+    code, info = pkv.pkv_get_device_error(clear=True)
+    if code:
+        raise RuntimeError(f"device error {code} ({pkv.DEVERR.get(code)}), info {info}")
+
+    cpu_baseline = None
+    if rank == 0 and cpu_arrays is not None:
+        gbs, rows, dt = time_oracle(wl, cpu_arrays, args.cpu_budget)
+        threads = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS") or "1"
+        cpu_baseline = {"value": gbs, "unit": "GB/s", "cores": int(threads), "kind": "oracle",
+                        "sample": f"{rows} sequences of the batch-64 decode workload, one at a time "
+                                  f"(KV scatter + fp64 gather-then-dense attention), {dt:.1f} s",
+                        "host_cpus": os.cpu_count()}
+    if dist is not None:
+        dist.barrier()
+    if rank == 0:
+        line = {"metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1))",
+                "config": head["config"], "roofline": head["roofline"], "cpu_baseline": cpu_baseline,
+                "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+                "secondary": secondary}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

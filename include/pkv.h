@@ -1,0 +1,227 @@
+/*
+ * pkv.h -- C ABI of libpkv: GQA attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * The library is the data-parallel hot path of a nano-vLLM-style inference
+ * step, as the pages describe it:
+ *
+ *   a1  pkv_slot_mapping     where each new token's K/V row lives in the pool
+ *   a2  pkv_store_kvcache    scatter the new K/V rows into the block pool
+ *   a3  pkv_prefill_varlen   varlen prefill attention, position-offset causal mask
+ *   a4  pkv_decode           single-token decode attention over the block tables
+ *   a5  pkv_sample           temperature sampling by exponential race
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is DEVICE memory owned by the caller, unless stated.
+ *   The library keeps no pointer after a call returns and frees nothing.
+ * - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *   NULL is the legacy default stream).  No call synchronises with the host,
+ *   reads device data on the host, or allocates device memory; scratch space
+ *   comes from a caller-provided workspace whose size a *_workspace_size call
+ *   reports.  `max_*` bounds are passed in for the same reason.
+ * - Host-checkable errors (null pointers, unsupported shapes, bad sizes) return
+ *   a non-zero pkv_status before anything is launched.  A failed launch
+ *   returns PKV_ERR_CUDA.  Errors only the device can see (a block id outside
+ *   the pool, a decreasing cu_seqlens, a temperature <= 0, a pipeline wait that
+ *   ran out) are recorded in a per-device error word read by
+ *   pkv_get_device_error(); the kernel then skips the offending access.
+ * - K/V pools are laid out [num_blocks, block_size, num_kv_heads, head_dim] in
+ *   bf16, one pool per layer for K and one for V.  Block tables are int32
+ *   [num_seqs, max_blocks_per_seq], row s listing sequence s's physical block
+ *   ids in logical order, padded with -1.  Supported: head_dim = 128,
+ *   block_size a multiple of 256, num_heads = 2 * num_kv_heads (two query
+ *   heads share each KV head, as in Qwen3-0.6B); anything else returns
+ *   PKV_ERR_UNSUPPORTED.
+ * - bf16 tensors are passed as pkv_bf16 (the raw 16-bit pattern).
+ *
+ * Citations name the page and the figure or section that defines the step.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t pkv_bf16;     /* raw bfloat16 bits */
+typedef void *pkv_stream_t;    /* cudaStream_t */
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent sizes */
+    PKV_ERR_UNSUPPORTED = 2,   /* shape or device outside the supported set */
+    PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    PKV_ERR_CUDA = 4           /* a CUDA runtime/driver call failed */
+} pkv_status;
+
+/* Device-side error codes (first one recorded wins). */
+enum {
+    PKV_DEVERR_NONE = 0,
+    PKV_DEVERR_BLOCK_ID = 1,     /* block table entry outside [0, num_blocks) */
+    PKV_DEVERR_SLOT = 2,         /* slot_mapping entry >= num_blocks * block_size */
+    PKV_DEVERR_SEQLENS = 3,      /* cu_seqlens decreasing, q_len > k_len, or a length above its max_* bound */
+    PKV_DEVERR_TEMPERATURE = 4,  /* temperature <= 0, inf or NaN */
+    PKV_DEVERR_TIMEOUT = 5,      /* an mbarrier wait exceeded its limit */
+    PKV_DEVERR_BLOCK_TABLE = 6   /* a position past max_blocks_per_seq * block_size */
+};
+
+/* ABI version; bumped on any signature change. */
+PKV_API int32_t pkv_abi_version(void);
+
+/* Human-readable name of a pkv_status.  Static storage; never NULL. */
+PKV_API const char *pkv_status_string(pkv_status status);
+
+/*
+ * a1. Slot of every new token.
+ * Visual atlas (diomchen.github.io/reference/visual-atlas.html), figure
+ * "T=5, block_size=2, block_table=[3,0,4]": slot = block_table[pos / bs] * bs
+ * + pos % bs.  The new tokens of sequence s are its last q_len positions:
+ * positions k_len - q_len .. k_len - 1 (atlas fig. 26: after a prefix hit the
+ * query is shorter than the keys; Nano-vLLM overview, Sequence counters: a
+ * decode feeds the one token without KV).
+ *
+ *   cu_seqlens_q  int32 [num_seqs + 1]; NULL means one new token per sequence
+ *                 (decode: token i belongs to sequence i, total_q == num_seqs)
+ *   cu_seqlens_k  int32 [num_seqs + 1] running key offsets, or NULL
+ *   context_lens  int32 [num_seqs] keys per sequence, or NULL; exactly one of
+ *                 cu_seqlens_k / context_lens is non-NULL
+ *   slot_mapping  int32 [total_q] output, packed token order.  A token whose
+ *                 position falls outside its block table gets -1 and
+ *                 PKV_DEVERR_BLOCK_TABLE / PKV_DEVERR_BLOCK_ID is recorded.
+ */
+PKV_API pkv_status pkv_slot_mapping(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            const int32_t *context_lens, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q,
+                            int32_t block_size, int32_t num_blocks, int32_t *slot_mapping,
+                            pkv_stream_t stream);
+
+/*
+ * a2. Scatter new K/V rows into the pools: k_cache[slot / bs, slot % bs] = k[i],
+ * v_cache likewise, for i < n_tokens.  nano-vLLM offline explainer
+ * (3479845.xyz/nano-vllm/nano-vllm-offline), accuracy & scope box: the input
+ * tokens write their KV first; interactive guide (blog-mushroom.pages.dev)
+ * ch. 08: the KV cache is written during attention.
+ *
+ *   k, v            bf16 [n_tokens, num_kv_heads, head_dim]; token i starts at
+ *                   element i * k_token_stride (resp. v_token_stride), which
+ *                   must be a multiple of 8 and >= num_kv_heads * head_dim
+ *                   (so k/v may be views into a fused QKV buffer)
+ *   slot_mapping    int32 [n_tokens]; slot < 0 skips the row (padding)
+ *   k_cache/v_cache bf16 pools, written in place
+ * A slot >= num_blocks * block_size is skipped and PKV_DEVERR_SLOT recorded.
+ * Bit-exact copy.  Rows with equal slots race (last writer unspecified).
+ */
+PKV_API pkv_status pkv_store_kvcache(const pkv_bf16 *k, const pkv_bf16 *v, int64_t n_tokens,
+                             int64_t k_token_stride, int64_t v_token_stride,
+                             const int32_t *slot_mapping, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
+                             int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                             int32_t head_dim, pkv_stream_t stream);
+
+/*
+ * a3. Varlen prefill attention over the paged cache.
+ * Visual atlas, figure "cu_seqlens=[0,3,5]" (packed requests), figs. 16-17
+ * (softmax(scale QK^T + mask) V; diagonal kept; a cached chunk keeps its
+ * position offset), fig. 18 (query heads share K/V heads), fig. 22 (blockwise
+ * evaluation without materialising scores).
+ *
+ * For sequence s with q_len = cu_seqlens_q[s+1]-cu_seqlens_q[s] and
+ * k_len = cu_seqlens_k[s+1]-cu_seqlens_k[s] (0 <= q_len <= k_len), query i
+ * (0-based) of head h attends to keys j <= i + (k_len - q_len) of KV head
+ * h / (num_heads / num_kv_heads), read from the pool through block_tables[s].
+ * The new tokens' K/V must already be in the pool (pkv_store_kvcache first),
+ * so one call serves prompts with and without a cached prefix.
+ *
+ *   q    bf16 [total_q, num_heads, head_dim] packed
+ *   out  bf16 [total_q, num_heads, head_dim] packed, written; rows of a
+ *        sequence with q_len = 0 do not exist
+ *   max_seqlen_q / max_seqlen_k  bounds on q_len / k_len (host-known)
+ *   workspace  may be NULL when pkv_prefill_workspace_size() returns 0
+ * Accumulation in fp32, probabilities rounded to bf16 for the PV product,
+ * output rounded to bf16 once.
+ */
+PKV_API size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_seqlen_q);
+
+PKV_API pkv_status pkv_prefill_varlen(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                              int32_t max_seqlen_k, int32_t num_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                              float softmax_scale, pkv_bf16 *out, void *workspace,
+                              size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * a4. Decode attention: one query token per sequence over its whole context.
+ * Visual atlas fig. 21 ("a decode step's real work": the newest token's KV is
+ * written, then attention runs over the history); Nano-vLLM overview,
+ * Sequence counters ([A,B,C] -> D): context_lens[b] counts every key the step
+ * attends to, including the token whose KV this step wrote.
+ *
+ * out[b, h] = softmax_j(scale * q[b,h] . k_j) v_j over j < context_lens[b],
+ * K/V head h / (num_heads / num_kv_heads), keys walked through
+ * block_tables[b].  A sequence with context_lens[b] == 0 gets a zero row.
+ *
+ *   q    bf16 [batch, num_heads, head_dim];  out bf16 [batch, num_heads, head_dim]
+ *   max_context_len  bound on context_lens (host-known); larger entries are
+ *        clamped to max_blocks_per_seq * block_size and PKV_DEVERR_SEQLENS recorded
+ *   workspace  >= pkv_decode_workspace_size(batch, num_heads, num_kv_heads,
+ *        head_dim) bytes on the current device, 256-byte aligned; its contents
+ *        need no initialisation and are scratch after the call
+ * The work is split over the GPU's warps into equal runs of KV; partial
+ * softmax states are merged in a fixed order, so results are deterministic.
+ */
+PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                                 int32_t head_dim);
+
+PKV_API pkv_status pkv_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                      const int32_t *context_lens, int32_t batch, int32_t max_context_len,
+                      int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t num_blocks, float softmax_scale,
+                      pkv_bf16 *out, void *workspace, size_t workspace_bytes,
+                      pkv_stream_t stream);
+
+/*
+ * a5. Temperature sampling by exponential race.
+ * Visual atlas fig. 23: the engine samples with temperature only, as an
+ * exponential race: winner = argmax_v p_v / e_v (= argmin e_v / p_v), with
+ * p = softmax(logits / T) and e_v ~ Exp(1); not argmax p.
+ *
+ * Noise (the pages leave the generator open): Philox4x32-10 (Salmon et al.,
+ * SC'11) with key (seed low 32, seed high 32) and counter (v / 4, row + offset
+ * low 32, (row + offset) >> 32, 0); word v % 4 = x gives
+ * u = (2 (x >> 9) + 1) 2^-24 and e_v = -ln u.  Since argmax p_v / e_v equals
+ * argmax (logits_v / T - ln e_v), the kernel evaluates that form in fp32 in a
+ * single pass over the logits; ties go to the lowest index.
+ *
+ *   logits        fp32 [batch, vocab], row b at logits + b * row_stride
+ *   temperatures  fp32 [batch], each > 0
+ *   out_ids       int64 [batch]; -1 for a row with an invalid temperature
+ *                 (PKV_DEVERR_TEMPERATURE recorded) or no finite logit
+ */
+PKV_API pkv_status pkv_sample(const float *logits, int32_t batch, int32_t vocab, int64_t row_stride,
+                      const float *temperatures, uint64_t seed, uint64_t offset,
+                      int64_t *out_ids, pkv_stream_t stream);
+
+/*
+ * Read (and optionally clear) the current device's error word.  HOST output
+ * pointers.  Synchronises the device.  code = PKV_DEVERR_*; info = a value
+ * describing where (e.g. the sequence or token index).
+ */
+PKV_API pkv_status pkv_get_device_error(int32_t *code, int32_t *info, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,276 @@
+"""Paged GQA attention for GB300 (sm_103a): Python binding of libpkv.
+
+The binding only marshals arguments: it checks tensor dtypes, devices and
+shapes, passes raw device pointers and the current CUDA stream to the C ABI
+(``include/pkv.h``), and turns a non-zero status into :class:`PkvError`.
+Every step of the path runs in the library's CUDA kernels.  There is no CPU
+fallback: if ``libpkv.so`` has not been built, :func:`load` raises.
+
+Build the library with ``python -m paged_kv_attention_29_gb300.build``.
+
+Functions carry the C names:
+
+=========================  ================================================
+``pkv_slot_mapping``       slot of each new token (block table lookup)
+``pkv_store_kvcache``      scatter new K/V rows into the paged pools
+``pkv_prefill_varlen``     varlen prefill attention with the offset causal mask
+``pkv_decode``             single-token decode attention over block tables
+``pkv_sample``             temperature sampling by exponential race
+=========================  ================================================
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
+    "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
+    "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error",
+    "decode_workspace", "DEVERR",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpkv.so")
+_lib: Optional[ctypes.CDLL] = None
+
+DEVERR = {0: "none", 1: "block id outside pool", 2: "slot outside pool", 3: "sequence lengths",
+          4: "temperature", 5: "pipeline wait timed out", 6: "position past block table"}
+
+_c_int32 = ctypes.c_int32
+_c_int64 = ctypes.c_int64
+_c_size = ctypes.c_size_t
+_c_ptr = ctypes.c_void_p
+_c_float = ctypes.c_float
+_c_u64 = ctypes.c_uint64
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {pkv_status_string(status)} ({status})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libpkv.so (once).  Raises if it was not built: there is no fallback."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is missing; build it with `python -m paged_kv_attention_29_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    sig = {
+        "pkv_abi_version": (_c_int32, []),
+        "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "pkv_slot_mapping": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_int32, _c_int32,
+                                            _c_int32, _c_int32, _c_ptr, _c_ptr]),
+        "pkv_store_kvcache": (ctypes.c_int, [_c_ptr, _c_ptr, _c_int64, _c_int64, _c_int64, _c_ptr, _c_ptr,
+                                             _c_ptr, _c_int32, _c_int32, _c_int32, _c_int32, _c_ptr]),
+        "pkv_prefill_workspace_size": (_c_size, [_c_int32] * 5),
+        "pkv_prefill_varlen": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_int32,
+                                              _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
+                                              _c_int32, _c_int32, _c_float, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+        "pkv_decode_workspace_size": (_c_size, [_c_int32] * 4),
+        "pkv_decode": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
+                                      _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_float, _c_ptr,
+                                      _c_ptr, _c_size, _c_ptr]),
+        "pkv_sample": (ctypes.c_int, [_c_ptr, _c_int32, _c_int32, _c_int64, _c_ptr, _c_u64, _c_u64, _c_ptr,
+                                      _c_ptr]),
+        "pkv_get_device_error": (ctypes.c_int, [ctypes.POINTER(_c_int32), ctypes.POINTER(_c_int32), _c_int32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, ndim=None, contiguous=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libpkv has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _raise(status: int, where: str):
+    if status != 0:
+        raise PkvError(status, where)
+
+
+# ---------------------------------------------------------------------------
+# API
+# ---------------------------------------------------------------------------
+
+def pkv_abi_version() -> int:
+    return int(load().pkv_abi_version())
+
+
+def pkv_status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def pkv_slot_mapping(block_tables: torch.Tensor, num_blocks: int, block_size: int,
+                     slot_mapping: torch.Tensor, *, cu_seqlens_q: Optional[torch.Tensor] = None,
+                     cu_seqlens_k: Optional[torch.Tensor] = None, context_lens: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """Fill ``slot_mapping`` (int32 [total_q]) with the slot of every new token."""
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(slot_mapping, "slot_mapping", torch.int32, 1)
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k), ("context_lens", context_lens)):
+        if t is not None:
+            _check(t, name, torch.int32, 1)
+    num_seqs = block_tables.shape[0]
+    _raise(load().pkv_slot_mapping(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(context_lens), _ptr(block_tables),
+                                   block_tables.shape[1], num_seqs, slot_mapping.shape[0], block_size, num_blocks,
+                                   _ptr(slot_mapping), _stream(stream)), "pkv_slot_mapping")
+    return slot_mapping
+
+
+def _pool_shape(k_cache: torch.Tensor):
+    _check(k_cache, "k_cache", torch.bfloat16, 4)
+    nb, bs, hkv, d = k_cache.shape
+    return nb, bs, hkv, d
+
+
+def pkv_store_kvcache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, stream=None) -> None:
+    """k_cache[slot // bs, slot % bs] = k[i] (and v) for every row i; slot < 0 skips."""
+    nb, bs, hkv, d = _pool_shape(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    for name, t in (("k", k), ("v", v)):
+        _check(t, name, torch.bfloat16, 3, contiguous=False)
+        if tuple(t.shape[1:]) != (hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [n, {hkv}, {d}] with contiguous rows")
+    _check(slot_mapping, "slot_mapping", torch.int32, 1)
+    n = k.shape[0]
+    if v.shape[0] != n or slot_mapping.shape[0] != n:
+        raise ValueError("k, v and slot_mapping disagree on the token count")
+    _raise(load().pkv_store_kvcache(_ptr(k), _ptr(v), n, k.stride(0), v.stride(0), _ptr(slot_mapping),
+                                    _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, _stream(stream)),
+           "pkv_store_kvcache")
+
+
+def pkv_prefill_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                               max_seqlen_q: int) -> int:
+    return int(load().pkv_prefill_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_seqlen_q))
+
+
+def pkv_prefill_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                       cu_seqlens_k: torch.Tensor, block_tables: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                       softmax_scale: float, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Varlen prefill attention over the paged cache (the new tokens' K/V already stored)."""
+    nb, bs, hkv, d = _pool_shape(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(q, "q", torch.bfloat16, 3)
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    total_q, hq, dq = q.shape
+    if dq != d:
+        raise ValueError("q head_dim differs from the pool's")
+    num_seqs = cu_seqlens_q.shape[0] - 1
+    if cu_seqlens_k.shape[0] != num_seqs + 1 or block_tables.shape[0] != num_seqs:
+        raise ValueError("cu_seqlens_q, cu_seqlens_k and block_tables disagree on the sequence count")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _raise(load().pkv_prefill_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                     _ptr(block_tables), block_tables.shape[1], num_seqs, total_q, int(max_seqlen_q),
+                                     int(max_seqlen_k), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
+                                     _ptr(workspace), ws_bytes, _stream(stream)), "pkv_prefill_varlen")
+    return out
+
+
+def pkv_decode_workspace_size(batch: int, num_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(load().pkv_decode_workspace_size(batch, num_heads, num_kv_heads, head_dim))
+
+
+def decode_workspace(batch: int, num_heads: int, num_kv_heads: int, head_dim: int, device=None) -> torch.Tensor:
+    """A uint8 device buffer of the size pkv_decode needs (256-byte aligned by the allocator)."""
+    n = pkv_decode_workspace_size(batch, num_heads, num_kv_heads, head_dim)
+    if n == 0:
+        raise PkvError(2, "pkv_decode_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+               context_lens: torch.Tensor, max_context_len: int, softmax_scale: float,
+               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """Decode attention: one query token per sequence over context_lens[b] cached keys."""
+    nb, bs, hkv, d = _pool_shape(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(q, "q", torch.bfloat16, 3)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    batch, hq, dq = q.shape
+    if dq != d or context_lens.shape[0] != batch or block_tables.shape[0] != batch:
+        raise ValueError("q, context_lens and block_tables disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3)
+    if workspace is None:
+        workspace = decode_workspace(batch, hq, hkv, d, q.device)
+    _check(workspace, "workspace", torch.uint8, 1)
+    _raise(load().pkv_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                             _ptr(context_lens), batch, int(max_context_len), hq, hkv, d, bs, nb,
+                             float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "pkv_decode")
+    return out
+
+
+def pkv_sample(logits: torch.Tensor, temperatures: torch.Tensor, seed: int, offset: int = 0,
+               out_ids: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Exponential-race temperature sampling; returns int64 ids [batch]."""
+    _check(logits, "logits", torch.float32, 2, contiguous=False)
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    _check(temperatures, "temperatures", torch.float32, 1)
+    batch, vocab = logits.shape
+    if out_ids is None:
+        out_ids = torch.empty(batch, dtype=torch.int64, device=logits.device)
+    _check(out_ids, "out_ids", torch.int64, 1)
+    _raise(load().pkv_sample(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures),
+                             int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(out_ids),
+                             _stream(stream)), "pkv_sample")
+    return out_ids
+
+
+def pkv_get_device_error(clear: bool = True):
+    """(code, info) of the current device's error word; synchronises the device."""
+    code = _c_int32(0)
+    info = _c_int32(0)
+    _raise(load().pkv_get_device_error(ctypes.byref(code), ctypes.byref(info), 1 if clear else 0),
+           "pkv_get_device_error")
+    return int(code.value), int(info.value)

@@ -1,0 +1,530 @@
+// a4: paged GQA decode attention (one query token per sequence).
+//
+// Visual atlas (diomchen.github.io/reference/visual-atlas.html) fig. 21: a
+// decode step attends the newest token over its whole cached history; fig. 18:
+// the two query heads of a group read one K/V head, which is loaded once for
+// both.  The whole step is HBM-bound (about 2 flops per KV byte), so the design
+// is about keeping every SM's share of HBM streaming:
+//
+// * Work partition.  The KV of the batch is cut into 32-token chunks, ordered
+//   (sequence, KV head, chunk).  The persistent grid's W warps each take one
+//   contiguous run of floor((w+1)T/W) - floor(wT/W) chunks, so every warp
+//   streams the same number of bytes whatever the length mix.  A run that
+//   crosses a (sequence, KV head) boundary flushes a partial softmax state
+//   (running max m, sum l, unnormalised o) for each piece.
+// * Per-warp TMA pipeline.  Each warp owns STAGES shared-memory stages of
+//   one chunk of K and V (8 KiB each, 32 tokens x 256 B rows of one KV head,
+//   cut out of the [num_blocks, block_size, Hkv, 128] pool by a 4-D tensor
+//   map).  Lane 0 keeps STAGES chunks in flight; an mbarrier per stage tracks
+//   arrival.  No cross-warp synchronisation in the main loop.
+// * Compute.  Lanes form 4 groups of 8; a group owns 8 tokens of the chunk and
+//   each lane 16 of the 128 head dimensions (two 16-byte pieces, so every
+//   quarter-warp shared load reads one contiguous 128-byte run: no bank
+//   conflicts).  Partial dot products for both heads are reduced across the 8
+//   lanes by a transposing butterfly (14 shuffles for 16 values), leaving one
+//   token's score per lane; the chunk max is a warp max; the online-softmax
+//   rescale of o happens once per chunk and only when the max moved.
+// * Combine.  A second kernel merges each (sequence, head)'s pieces in warp
+//   order with the log-sum-exp rule, so the result does not depend on timing.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int D = kHeadDim;
+constexpr int G = kGroup;
+constexpr int CHUNK = 32;                  // tokens per stage
+constexpr int STAGES = 3;                  // stages per warp
+constexpr int WARPS = 4;                   // warps per CTA
+constexpr int KV_TILE_BYTES = CHUNK * D * 2;
+constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;
+constexpr int MAX_BATCH = 4096;
+constexpr int THREADS = WARPS * 32;
+
+constexpr size_t kStageRegion = static_cast<size_t>(WARPS) * STAGES * STAGE_BYTES;
+
+struct Params {
+    const uint16_t* q;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int max_blocks;
+    int batch;
+    int num_kv_heads;
+    int block_size;
+    int num_blocks;
+    float scale_log2;      // softmax scale * log2(e): scores live in the exp2 domain
+    int total_warps;
+    int32_t* plan;         // [batch + 1] chunk prefix per sequence (per KV head)
+    float* part_ml;        // [pieces][G][2]  (m, l)
+    float* part_o;         // [pieces][G][D]
+    int* err;
+};
+
+__device__ __forceinline__ int seq_chunks(const int32_t* prefix, int b) { return prefix[b + 1] - prefix[b]; }
+
+// Largest b with hkv * prefix[b] <= i  (prefix non-decreasing, prefix[0] = 0).
+__device__ __forceinline__ int locate_seq(const int32_t* prefix, int batch, int hkv, int64_t i) {
+    int lo = 0, hi = batch;      // invariant: hkv*prefix[lo] <= i < hkv*prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(hkv) * prefix[mid] <= i) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+struct Cursor {
+    int b, g, c, n;   // sequence, KV head, chunk within (b, g), chunks of b
+};
+
+__device__ __forceinline__ Cursor cursor_at(const int32_t* prefix, int batch, int hkv, int64_t i) {
+    Cursor cu;
+    cu.b = locate_seq(prefix, batch, hkv, i);
+    cu.n = seq_chunks(prefix, cu.b);
+    const int64_t rem = i - static_cast<int64_t>(hkv) * prefix[cu.b];
+    cu.g = static_cast<int>(rem / cu.n);
+    cu.c = static_cast<int>(rem - static_cast<int64_t>(cu.g) * cu.n);
+    return cu;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& cu, const int32_t* prefix, int batch, int hkv) {
+    if (++cu.c < cu.n) return;
+    cu.c = 0;
+    if (++cu.g < hkv) return;
+    cu.g = 0;
+    do { ++cu.b; } while (cu.b < batch && seq_chunks(prefix, cu.b) == 0);
+    cu.n = cu.b < batch ? seq_chunks(prefix, cu.b) : 0;
+}
+
+__device__ __forceinline__ void load_q(const Params& p, int b, int g, int r, float (&qf)[G][16]) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        const uint16_t* row = p.q + (static_cast<int64_t>(b) * (p.num_kv_heads * G) + g * G + h) * D;
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(row + 8 * r));
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(row + 64 + 8 * r));
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            qf[h][2 * e] = bf16_lo(w[e]) * p.scale_log2;
+            qf[h][2 * e + 1] = bf16_hi(w[e]) * p.scale_log2;
+        }
+    }
+}
+
+__device__ __forceinline__ float dot16(const float (&qh)[16], const uint4& a, const uint4& c) {
+    float s0 = 0.f, s1 = 0.f;
+    s0 = fmaf(qh[0], bf16_lo(a.x), s0);  s1 = fmaf(qh[1], bf16_hi(a.x), s1);
+    s0 = fmaf(qh[2], bf16_lo(a.y), s0);  s1 = fmaf(qh[3], bf16_hi(a.y), s1);
+    s0 = fmaf(qh[4], bf16_lo(a.z), s0);  s1 = fmaf(qh[5], bf16_hi(a.z), s1);
+    s0 = fmaf(qh[6], bf16_lo(a.w), s0);  s1 = fmaf(qh[7], bf16_hi(a.w), s1);
+    s0 = fmaf(qh[8], bf16_lo(c.x), s0);  s1 = fmaf(qh[9], bf16_hi(c.x), s1);
+    s0 = fmaf(qh[10], bf16_lo(c.y), s0); s1 = fmaf(qh[11], bf16_hi(c.y), s1);
+    s0 = fmaf(qh[12], bf16_lo(c.z), s0); s1 = fmaf(qh[13], bf16_hi(c.z), s1);
+    s0 = fmaf(qh[14], bf16_lo(c.w), s0); s1 = fmaf(qh[15], bf16_hi(c.w), s1);
+    return s0 + s1;
+}
+
+__device__ __forceinline__ void axpy16(float (&oh)[16], float pw, const uint4& a, const uint4& c) {
+    oh[0] = fmaf(pw, bf16_lo(a.x), oh[0]);   oh[1] = fmaf(pw, bf16_hi(a.x), oh[1]);
+    oh[2] = fmaf(pw, bf16_lo(a.y), oh[2]);   oh[3] = fmaf(pw, bf16_hi(a.y), oh[3]);
+    oh[4] = fmaf(pw, bf16_lo(a.z), oh[4]);   oh[5] = fmaf(pw, bf16_hi(a.z), oh[5]);
+    oh[6] = fmaf(pw, bf16_lo(a.w), oh[6]);   oh[7] = fmaf(pw, bf16_hi(a.w), oh[7]);
+    oh[8] = fmaf(pw, bf16_lo(c.x), oh[8]);   oh[9] = fmaf(pw, bf16_hi(c.x), oh[9]);
+    oh[10] = fmaf(pw, bf16_lo(c.y), oh[10]); oh[11] = fmaf(pw, bf16_hi(c.y), oh[11]);
+    oh[12] = fmaf(pw, bf16_lo(c.z), oh[12]); oh[13] = fmaf(pw, bf16_hi(c.z), oh[13]);
+    oh[14] = fmaf(pw, bf16_lo(c.w), oh[14]); oh[15] = fmaf(pw, bf16_hi(c.w), oh[15]);
+}
+
+// Write one piece's partial state (m, l, o) for both heads of the group.
+__device__ __forceinline__ void flush_piece(const Params& p, int slot, int lane, const float (&m)[G],
+                                            const float (&l)[G], float (&o)[G][16]) {
+    float lsum[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        lsum[h] = l[h];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], off);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], 8);
+            o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], 16);
+        }
+    }
+    if (lane < 8) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float* dst = p.part_o + (static_cast<int64_t>(slot) * G + h) * D;
+            float4* d0 = reinterpret_cast<float4*>(dst + 8 * lane);
+            float4* d1 = reinterpret_cast<float4*>(dst + 64 + 8 * lane);
+            d0[0] = make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+            d0[1] = make_float4(o[h][4], o[h][5], o[h][6], o[h][7]);
+            d1[0] = make_float4(o[h][8], o[h][9], o[h][10], o[h][11]);
+            d1[1] = make_float4(o[h][12], o[h][13], o[h][14], o[h][15]);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            p.part_ml[(static_cast<int64_t>(slot) * G + h) * 2 + 0] = m[h];
+            p.part_ml[(static_cast<int64_t>(slot) * G + h) * 2 + 1] = lsum[h];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1 KiB-aligned base
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageRegion);
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + kStageRegion + WARPS * STAGES * 8);
+    int32_t* tsum = prefix + (p.batch + 1);
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int hkv = p.num_kv_heads;
+    const int cap = p.max_blocks * p.block_size;
+
+    // ---- chunk counts per sequence and their prefix (every CTA computes the same)
+    const int per = (p.batch + THREADS - 1) / THREADS;
+    const int b0 = tid * per;
+    int local = 0;
+    for (int b = b0; b < min(p.batch, b0 + per); ++b) {
+        int L = __ldg(p.context_lens + b);
+        if (L < 0 || L > cap) {
+            if (blockIdx.x == 0) record_error(p.err, PKV_DEVERR_SEQLENS, b);
+            L = L < 0 ? 0 : cap;
+        }
+        local += (L + CHUNK - 1) / CHUNK;
+    }
+    tsum[tid] = local;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int t = 0; t < THREADS; ++t) { const int x = tsum[t]; tsum[t] = run; run += x; }
+        prefix[p.batch] = run;
+    }
+    __syncthreads();
+    {
+        int run = tsum[tid];
+        for (int b = b0; b < min(p.batch, b0 + per); ++b) {
+            prefix[b] = run;
+            int L = __ldg(p.context_lens + b);
+            L = L < 0 ? 0 : (L > cap ? cap : L);
+            run += (L + CHUNK - 1) / CHUNK;
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int b = tid; b <= p.batch; b += THREADS) p.plan[b] = prefix[b];
+    }
+
+    // ---- this warp's run of chunks
+    const int W = p.total_warps;
+    const int gw = blockIdx.x * WARPS + warp;
+    const int64_t total = static_cast<int64_t>(hkv) * prefix[p.batch];
+    const int64_t begin = static_cast<int64_t>(gw) * total / W;
+    const int64_t end = static_cast<int64_t>(gw + 1) * total / W;
+    if (begin >= end) return;
+    const int n_mine = static_cast<int>(end - begin);
+
+    uint8_t* my_stages = smem + static_cast<size_t>(warp) * STAGES * STAGE_BYTES;
+    const uint32_t stage_base = smem_u32(my_stages);
+    const uint32_t bar_base = smem_u32(bars + warp * STAGES);
+    if (lane == 0) {
+        for (int s = 0; s < STAGES; ++s) mbar_init(bar_base + 8 * s, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    __syncwarp();
+    const uint64_t policy = l2_policy_evict_first();
+
+    // ---- producer state: its own cursor and a window of 32 block-table entries
+    Cursor pc = cursor_at(prefix, p.batch, hkv, begin);
+    int bt_b = -1, bt_base = 0, bt_lane = -1;
+    int issued = 0;
+    auto issue_next = [&]() {
+        const int tok = pc.c * CHUNK;
+        const int j = tok / p.block_size;
+        if (pc.b != bt_b || j < bt_base || j >= bt_base + 32) {
+            bt_b = pc.b;
+            bt_base = j;
+            const int jj = bt_base + lane;
+            bt_lane = jj < p.max_blocks ? __ldg(p.block_tables + static_cast<int64_t>(pc.b) * p.max_blocks + jj) : -1;
+        }
+        const int phys = __shfl_sync(0xffffffffu, bt_lane, j - bt_base);
+        if (lane == 0) {
+            if (phys < 0 || phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, pc.b);
+            const int s = issued % STAGES;
+            const uint32_t bar = bar_base + 8 * s;
+            const uint32_t dst = stage_base + s * STAGE_BYTES;
+            mbar_arrive_expect_tx(bar, STAGE_BYTES);
+            const int off = tok - j * p.block_size;
+            tma_load_4d_hint(dst, &tm_k, bar, 0, pc.g, off, phys, policy);
+            tma_load_4d_hint(dst + KV_TILE_BYTES, &tm_v, bar, 0, pc.g, off, phys, policy);
+        }
+        ++issued;
+        cursor_next(pc, prefix, p.batch, hkv);
+    };
+    const int prologue = n_mine < STAGES ? n_mine : STAGES;
+    for (int i = 0; i < prologue; ++i) issue_next();
+
+    // ---- consumer
+    const int grp = lane >> 3;       // token group: tokens grp + 4i of the chunk
+    const int r = lane & 7;          // 16 head dims: [8r, 8r+8) and [64+8r, 64+8r+8)
+    Cursor cc = cursor_at(prefix, p.batch, hkv, begin);
+    float qf[G][16], o[G][16], m[G], l[G];
+    load_q(p, cc.b, cc.g, r, qf);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[h][e] = 0.f;
+    }
+    int Lb = min(max(__ldg(p.context_lens + cc.b), 0), cap);
+    bool failed = false;
+    int consumed = 0;
+
+    for (int k = 0; k < n_mine; ++k) {
+        const int s = k % STAGES;
+        const bool ok = mbar_wait(bar_base + 8 * s, (k / STAGES) & 1, p.err, gw);
+        if (__any_sync(0xffffffffu, !ok)) { failed = true; break; }   // warp-uniform exit
+        const uint32_t kb = stage_base + s * STAGE_BYTES;
+        const uint32_t vb = kb + KV_TILE_BYTES;
+        const int n_valid = min(CHUNK, Lb - cc.c * CHUNK);
+
+        // scores: partial dot products of this lane's 16 dims, 8 tokens, 2 heads
+        float part[8][G];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t row = kb + (grp + 4 * i) * (D * 2);
+            const uint4 a = ld_shared_v4(row + 16 * r);
+            const uint4 c = ld_shared_v4(row + 128 + 16 * r);
+#pragma unroll
+            for (int h = 0; h < G; ++h) part[i][h] = dot16(qf[h], a, c);
+        }
+        // transposing butterfly over the 8 lanes of the group: lane r ends with token grp + 4r
+        float a4[4][G], a2[2][G], sc[G];
+        const bool hA = (r & 4) != 0, hB = (r & 2) != 0, hC = (r & 1) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float send = hA ? part[j][h] : part[j + 4][h];
+                const float keep = hA ? part[j + 4][h] : part[j][h];
+                a4[j][h] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+            }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float send = hB ? a4[j][h] : a4[j + 2][h];
+                const float keep = hB ? a4[j + 2][h] : a4[j][h];
+                a2[j][h] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+            }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float send = hC ? a2[0][h] : a2[1][h];
+            const float keep = hC ? a2[1][h] : a2[0][h];
+            sc[h] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        }
+        const bool valid = (grp + 4 * r) < n_valid;
+        float pr[G];
+        bool moved = false;
+        float alpha[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float sv = valid ? sc[h] : -INFINITY;
+            float cm = sv;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+            const float m_new = fmaxf(m[h], cm);
+            alpha[h] = exp2f(m[h] - m_new);
+            moved |= (m_new != m[h]);
+            m[h] = m_new;
+            pr[h] = exp2f(sv - m_new);
+            l[h] = fmaf(l[h], alpha[h], pr[h]);
+        }
+        if (moved) {
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[h][e] *= alpha[h];
+        }
+        // o += p v over the group's 8 tokens
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float pw[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) pw[h] = __shfl_sync(0xffffffffu, pr[h], (lane & ~7) | i);
+            if (grp + 4 * i < n_valid) {
+                const uint32_t row = vb + (grp + 4 * i) * (D * 2);
+                const uint4 a = ld_shared_v4(row + 16 * r);
+                const uint4 c = ld_shared_v4(row + 128 + 16 * r);
+#pragma unroll
+                for (int h = 0; h < G; ++h) axpy16(o[h], pw[h], a, c);
+            }
+        }
+        __syncwarp();
+        ++consumed;
+        if (issued < n_mine) issue_next();
+
+        // end of this (sequence, KV head) piece or of the warp's run
+        if (cc.c == cc.n - 1 || k == n_mine - 1) {
+            flush_piece(p, cc.b * hkv + cc.g + gw, lane, m, l, o);
+            if (k != n_mine - 1) {
+                cursor_next(cc, prefix, p.batch, hkv);
+                load_q(p, cc.b, cc.g, r, qf);
+                Lb = min(max(__ldg(p.context_lens + cc.b), 0), cap);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    m[h] = -INFINITY;
+                    l[h] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[h][e] = 0.f;
+                }
+            }
+        } else {
+            ++cc.c;
+        }
+    }
+    if (failed) {
+        // let this warp's copies in flight land before the CTA's shared memory goes away
+        for (int k = consumed; k < issued; ++k) {
+            const bool ok = mbar_wait(bar_base + 8 * (k % STAGES), (k / STAGES) & 1, p.err, gw);
+            if (__any_sync(0xffffffffu, !ok)) break;
+        }
+    }
+}
+
+// One warp per (sequence, query head): merge its pieces in warp order.
+__global__ void __launch_bounds__(128)
+decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int idx = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (idx >= p.batch * num_heads) return;
+    const int b = idx / num_heads;
+    const int h = idx - b * num_heads;
+    const int g = h / G;
+    const int hh = h - g * G;
+    const int hkv = p.num_kv_heads;
+    const int n = p.plan[b + 1] - p.plan[b];
+    uint16_t* dst = out + static_cast<int64_t>(idx) * D + 4 * lane;
+    if (n == 0) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        return;
+    }
+    const int64_t W = p.total_warps;
+    const int64_t total = static_cast<int64_t>(hkv) * p.plan[p.batch];
+    const int64_t start = static_cast<int64_t>(hkv) * p.plan[b] + static_cast<int64_t>(g) * n;
+    const int64_t last = start + n - 1;
+    const int wf = static_cast<int>(((start + 1) * W - 1) / total);
+    const int wl = static_cast<int>(((last + 1) * W - 1) / total);
+    const int q = b * hkv + g;
+    // when the grid has more warps than chunks, some warps between wf and wl own
+    // nothing and left no piece: skip them
+    auto owns_chunks = [&](int w) {
+        return (static_cast<int64_t>(w + 1) * total) / W > (static_cast<int64_t>(w) * total) / W;
+    };
+    float M = -INFINITY;
+    for (int w = wf; w <= wl; ++w)
+        if (owns_chunks(w)) M = fmaxf(M, p.part_ml[(static_cast<int64_t>(q + w) * G + hh) * 2]);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = wf; w <= wl; ++w) {
+        if (!owns_chunks(w)) continue;
+        const int64_t slot = static_cast<int64_t>(q + w) * G + hh;
+        const float sc = exp2f(p.part_ml[slot * 2] - M);
+        L = fmaf(sc, p.part_ml[slot * 2 + 1], L);
+        const float4 v = *reinterpret_cast<const float4*>(p.part_o + slot * D + 4 * lane);
+        acc.x = fmaf(sc, v.x, acc.x);
+        acc.y = fmaf(sc, v.y, acc.y);
+        acc.z = fmaf(sc, v.z, acc.z);
+        acc.w = fmaf(sc, v.w, acc.w);
+    }
+    const float inv = 1.f / L;
+    uint2 packed;
+    packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) = packed;
+}
+
+size_t dynamic_smem_bytes(int batch) {
+    return kStageRegion + WARPS * STAGES * 8 + static_cast<size_t>(batch + 1) * 4 + THREADS * 4 + 1024;
+}
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+int decode_total_warps() { return sm_count() * WARPS; }
+
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int total_warps) {
+    const size_t pieces = static_cast<size_t>(batch) * num_kv_heads + total_warps;
+    return align256(static_cast<size_t>(batch + 1) * 4) + align256(pieces * G * 2 * 4) +
+           align256(pieces * G * D * 4);
+}
+
+pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream) {
+    if (a.batch > MAX_BATCH) return PKV_ERR_UNSUPPORTED;
+    const int W = decode_total_warps();
+    if (W <= 0) return PKV_ERR_CUDA;
+    const size_t need = decode_workspace_bytes(a.batch, a.num_kv_heads, W);
+    if (a.workspace == nullptr || a.workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (a.batch == 0) return PKV_OK;
+
+    CUtensorMap tm_k, tm_v;
+    const uint64_t dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_kv_heads),
+                              static_cast<uint64_t>(a.block_size), static_cast<uint64_t>(a.num_blocks)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.num_kv_heads) * D * 2,
+                                 static_cast<uint64_t>(a.block_size) * a.num_kv_heads * D * 2};
+    const uint32_t box[4] = {static_cast<uint32_t>(D), 1u, static_cast<uint32_t>(CHUNK), 1u};
+    if (encode_tiled(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(a.k_cache), dims,
+                     strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_INVALID_ARG;
+    if (encode_tiled(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(a.v_cache), dims,
+                     strides, box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return PKV_ERR_INVALID_ARG;
+
+    Params p;
+    p.q = a.q;
+    p.block_tables = a.block_tables;
+    p.context_lens = a.context_lens;
+    p.max_blocks = a.max_blocks;
+    p.batch = a.batch;
+    p.num_kv_heads = a.num_kv_heads;
+    p.block_size = a.block_size;
+    p.num_blocks = a.num_blocks;
+    p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+    p.total_warps = W;
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    const size_t pieces = static_cast<size_t>(a.batch) * a.num_kv_heads + W;
+    p.plan = reinterpret_cast<int32_t*>(ws);
+    ws += align256(static_cast<size_t>(a.batch + 1) * 4);
+    p.part_ml = reinterpret_cast<float*>(ws);
+    ws += align256(pieces * G * 2 * 4);
+    p.part_o = reinterpret_cast<float*>(ws);
+    p.err = err;
+
+    const size_t smem = dynamic_smem_bytes(a.batch);
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(decode_splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(dynamic_smem_bytes(MAX_BATCH))) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_device = dev;
+    }
+    decode_splitk_kernel<<<W / WARPS, THREADS, smem, stream>>>(tm_k, tm_v, p);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    const int n_rows = a.batch * a.num_heads;
+    decode_combine_kernel<<<(n_rows + 3) / 4, 128, 0, stream>>>(p, a.num_heads, a.out);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+}  // namespace pkv

@@ -1,0 +1,90 @@
+// Host-side declarations shared by the libpkv translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kHeadDim = 128;
+constexpr int kGroup = 2;            // query heads per KV head
+constexpr int kBlockQuantum = 256;   // block_size must be a multiple of this
+
+// Device address of the current device's error word (int[2]); nullptr on failure.
+int* device_error_word();
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle);
+
+// ---- a1 / a2 --------------------------------------------------------------
+cudaError_t launch_slot_mapping(const int32_t* cu_q, const int32_t* cu_k, const int32_t* ctx,
+                                const int32_t* block_tables, int max_blocks, int num_seqs,
+                                int total_q, int block_size, int num_blocks, int32_t* slots,
+                                int* err, cudaStream_t stream);
+
+cudaError_t launch_store_kvcache(const uint16_t* k, const uint16_t* v, int64_t n_tokens,
+                                 int64_t k_stride, int64_t v_stride, const int32_t* slots,
+                                 uint16_t* k_cache, uint16_t* v_cache, int64_t num_slots,
+                                 int row_elems, int* err, cudaStream_t stream);
+
+// ---- a4 ---------------------------------------------------------------------
+struct DecodeArgs {
+    const uint16_t* q;
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    uint16_t* out;
+    int max_blocks;
+    int batch;
+    int num_heads;
+    int num_kv_heads;
+    int block_size;
+    int num_blocks;
+    float softmax_scale;
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+int decode_total_warps();                                  // warps the decode grid runs
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int total_warps);
+pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream);
+
+// ---- a3 ---------------------------------------------------------------------
+struct PrefillArgs {
+    const uint16_t* q;
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    const int32_t* block_tables;
+    uint16_t* out;
+    int max_blocks;
+    int num_seqs;
+    int total_q;
+    int max_seqlen_q;
+    int max_seqlen_k;
+    int num_heads;
+    int num_kv_heads;
+    int block_size;
+    int num_blocks;
+    float softmax_scale;
+};
+
+pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream);
+
+// ---- a5 ---------------------------------------------------------------------
+cudaError_t launch_sample(const float* logits, int batch, int vocab, int64_t row_stride,
+                          const float* temperatures, uint64_t seed, uint64_t offset,
+                          int64_t* out_ids, int* err, cudaStream_t stream);
+
+}  // namespace pkv

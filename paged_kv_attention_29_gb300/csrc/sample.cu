@@ -1,0 +1,164 @@
+// a5: temperature sampler by exponential race.
+//
+// Visual atlas (diomchen.github.io/reference/visual-atlas.html) fig. 23: the
+// sampler's winner is argmax_v p_v / e_v with p = softmax(logits / T) and
+// e_v ~ Exp(1) (equivalently argmin e_v / p_v); it is not argmax p.
+//
+// Because p_v = exp(logits_v / T - c) for a row constant c, the winner is
+// also argmax_v (logits_v / T - ln e_v): one pass over the logits, no softmax
+// normalisation.  Each row is cut into 8 slices, one per CTA of a thread-block
+// cluster; a CTA reduces its slice to (best key, lowest index), and the
+// cluster's first CTA merges the 8 results through distributed shared memory,
+// so no global scratch or second launch is needed.
+//
+// Noise: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11), one call per 4
+// consecutive columns: counter (column / 4, row + offset low, row + offset
+// high, 0), key (seed low, seed high).  Word x of a column gives
+// u = (2 (x >> 9) + 1) 2^-24, exact in fp32 and strictly inside (0, 1), and
+// e = -ln u > 0.
+#include <cooperative_groups.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace pkv {
+namespace {
+
+constexpr int CLUSTER = 8;
+constexpr int THREADS = 256;
+
+// Philox4x32 round constants from the SC'11 paper (multipliers and Weyl increments).
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round) {
+            k0 += kPhiloxW0;
+            k1 += kPhiloxW1;
+        }
+        const uint32_t lo0 = kPhiloxM0 * c.x;
+        const uint32_t hi0 = __umulhi(kPhiloxM0, c.x);
+        const uint32_t lo1 = kPhiloxM1 * c.z;
+        const uint32_t hi1 = __umulhi(kPhiloxM1, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// (key, index) with "better" = larger key, then lower index; index < 0 = none.
+__device__ __forceinline__ bool better(float k, int i, float bk, int bi) {
+    if (i < 0) return false;
+    if (bi < 0) return true;
+    return (k > bk) || (k == bk && i < bi);
+}
+
+__device__ __forceinline__ void consider(float logit, float inv_t, uint32_t x, int col, float& bk, int& bi) {
+    const float u = __uint2float_rn(2u * (x >> 9) + 1u) * 5.9604644775390625e-08f;   // 2^-24
+    const float e = -logf(u);
+    const float key = logit * inv_t - logf(e);
+    // NaN keys never win; a -inf key only wins against nothing and is rejected
+    if (key == key && key > -INFINITY && better(key, col, bk, bi)) {
+        bk = key;
+        bi = col;
+    }
+}
+
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS)
+sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stride,
+                   const float* __restrict__ temperatures, uint32_t key0, uint32_t key1,
+                   uint64_t offset, int vec_ok, int64_t* __restrict__ out_ids, int* err) {
+    __shared__ float s_key[THREADS / 32];
+    __shared__ int s_idx[THREADS / 32];
+    __shared__ float c_key;
+    __shared__ int c_idx;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int row = blockIdx.y;
+    const int tid = threadIdx.x;
+    const float T = __ldg(temperatures + row);
+    const bool t_ok = (T > 0.f) && (T < INFINITY);
+
+    float bk = -INFINITY;
+    int bi = -1;
+    if (t_ok) {
+        const float inv_t = 1.0f / T;
+        const uint64_t rr = static_cast<uint64_t>(row) + offset;
+        const uint32_t c1 = static_cast<uint32_t>(rr);
+        const uint32_t c2 = static_cast<uint32_t>(rr >> 32);
+        const float* lrow = logits + static_cast<int64_t>(row) * row_stride;
+        const int nquads = (vocab + 3) >> 2;
+        const int per = (nquads + CLUSTER - 1) / CLUSTER;
+        const int q0 = rank * per;
+        const int q1 = min(nquads, q0 + per);
+        for (int qd = q0 + tid; qd < q1; qd += THREADS) {
+            const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(qd), c1, c2, 0u), key0, key1);
+            const int col = qd * 4;
+            if (vec_ok && col + 3 < vocab) {
+                const float4 l4 = __ldcs(reinterpret_cast<const float4*>(lrow + col));
+                consider(l4.x, inv_t, x.x, col, bk, bi);
+                consider(l4.y, inv_t, x.y, col + 1, bk, bi);
+                consider(l4.z, inv_t, x.z, col + 2, bk, bi);
+                consider(l4.w, inv_t, x.w, col + 3, bk, bi);
+            } else {
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < vocab) consider(__ldcs(lrow + col + e), inv_t, xs[e], col + e, bk, bi);
+            }
+        }
+    } else if (rank == 0 && tid == 0) {
+        record_error(err, PKV_DEVERR_TEMPERATURE, row);
+    }
+    // warp, then CTA reduction
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, bk, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
+    }
+    if ((tid & 31) == 0) { s_key[tid >> 5] = bk; s_idx[tid >> 5] = bi; }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < THREADS / 32; ++w)
+            if (better(s_key[w], s_idx[w], bk, bi)) { bk = s_key[w]; bi = s_idx[w]; }
+        c_key = bk;
+        c_idx = bi;
+    }
+    // cluster reduction through distributed shared memory
+    cluster.sync();
+    if (rank == 0 && tid == 0) {
+        float k = c_key;
+        int i = c_idx;
+        for (int r = 1; r < CLUSTER; ++r) {
+            const float rk = *cluster.map_shared_rank(&c_key, r);
+            const int ri = *cluster.map_shared_rank(&c_idx, r);
+            if (better(rk, ri, k, i)) { k = rk; i = ri; }
+        }
+        out_ids[row] = t_ok ? static_cast<int64_t>(i) : -1;
+    }
+    cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
+}
+
+}  // namespace
+
+cudaError_t launch_sample(const float* logits, int batch, int vocab, int64_t row_stride,
+                          const float* temperatures, uint64_t seed, uint64_t offset,
+                          int64_t* out_ids, int* err, cudaStream_t stream) {
+    if (batch == 0) return cudaSuccess;
+    const int vec_ok = ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) && (row_stride % 4 == 0);
+    dim3 grid(CLUSTER, batch);
+    sample_race_kernel<<<grid, THREADS, 0, stream>>>(logits, vocab, row_stride, temperatures,
+                                                     static_cast<uint32_t>(seed),
+                                                     static_cast<uint32_t>(seed >> 32), offset, vec_ok,
+                                                     out_ids, err);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,80 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every symbol that
+include/pkv.h declares.  Host-side argument checks are exercised only where
+they return before any CUDA call (no GPU here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_attention_29_gb300 import build
+    build.build()
+    import paged_kv_attention_29_gb300 as pkv
+    return pkv.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]*?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_symbols()
+    for must in ["pkv_slot_mapping", "pkv_store_kvcache", "pkv_prefill_varlen", "pkv_decode", "pkv_sample",
+                 "pkv_decode_workspace_size", "pkv_get_device_error", "pkv_status_string"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_build_targets_sm103a_only():
+    from paged_kv_attention_29_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    import paged_kv_attention_29_gb300 as pkv
+    assert pkv.pkv_status_string(0) == "PKV_OK"
+    assert pkv.pkv_status_string(3) == "PKV_ERR_WORKSPACE"
+    assert pkv.pkv_abi_version() == 1
+
+
+def test_host_argument_checks_return_before_launch(lib):
+    P = None
+    # store: negative token count; row stride smaller than a row
+    assert lib.pkv_store_kvcache(P, P, -1, 1024, 1024, P, P, P, 4, 256, 8, 128, P) == 1
+    assert lib.pkv_store_kvcache(P, P, 4, 512, 1024, P, P, P, 4, 256, 8, 128, P) == 1
+    # decode: unsupported head_dim / group / block size
+    assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 8, 64, 256, 4, 0.1, P, P, 0, P) == 2
+    assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 4, 128, 256, 4, 0.1, P, P, 0, P) == 2
+    assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 8, 128, 100, 4, 0.1, P, P, 0, P) == 2
+    # prefill: max_seqlen_q > max_seqlen_k
+    assert lib.pkv_prefill_varlen(P, P, P, P, P, P, 4, 2, 10, 9, 8, 16, 8, 128, 256, 4, 0.1, P, P, 0, P) == 1
+    # slot mapping: both or neither of cu_seqlens_k / context_lens
+    assert lib.pkv_slot_mapping(P, P, P, P, 4, 2, 2, 256, 4, P, P) == 1
+    # sample: row stride below vocab, empty vocab
+    assert lib.pkv_sample(P, 2, 100, 50, P, 0, 0, P, P) == 1
+    assert lib.pkv_sample(P, 2, 0, 0, P, 0, 0, P, P) == 1
+    # zero-size calls are no-ops
+    assert lib.pkv_store_kvcache(P, P, 0, 1024, 1024, P, P, P, 4, 256, 8, 128, P) == 0
+    assert lib.pkv_sample(P, 0, 10, 10, P, 0, 0, P, P) == 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import paged_kv_attention_29_gb300 as pkv
+    x = torch.zeros(4, 8, 128, dtype=torch.bfloat16)
+    pool = torch.zeros(2, 256, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkv.pkv_store_kvcache(x, x, torch.zeros(4, dtype=torch.int32), pool, pool)

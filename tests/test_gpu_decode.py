@@ -1,0 +1,114 @@
+"""a4 decode attention on the GPU against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import paged_attention as pa
+from pkv_testutil import GpuBatch, assert_attention_close, bits, expect_no_device_error, f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["tiny-decode", "decode-b64", "long-decode"])
+def test_decode_configs_all_rows(pkv, name):
+    """Write the new token's K/V through the slot mapping, then decode; every row vs the oracle."""
+    wl = W.ALL[name]()
+    b = GpuBatch(wl, W.paged_values(wl))
+    b.run_slots_and_store(pkv, decode=True)
+    out = b.run_decode(pkv)
+    ref = b.oracle_decode()
+    assert_attention_close(out, ref, name)
+    expect_no_device_error(pkv)
+
+
+def _decode_only(pkv, kv_lens, seed, poison=False, pool_factor=1.25):
+    """Decode over a seeded pool without a store step (lengths may be 0)."""
+    kv_lens = np.asarray(kv_lens, dtype=np.int32)
+    wl = W.build_workload("edge", np.ones_like(kv_lens), kv_lens, seed, pool_factor=pool_factor)
+    vals = W.paged_values(wl, poison_unreferenced=poison)
+    if poison:   # every slot a sequence has not reached holds NaN as well
+        for s, L in enumerate(kv_lens):
+            nblk = -(-int(L) // wl.block_size)
+            for pos in range(int(L), nblk * wl.block_size):
+                blk, off = divmod(pa.slot_of(wl.block_tables[s], pos, wl.block_size), wl.block_size)
+                vals.k_cache[blk, off] = float("nan")
+                vals.v_cache[blk, off] = float("nan")
+    b = GpuBatch(wl, vals)
+    out = b.run_decode(pkv)
+    ref = pa.decode(f32(vals.q), f32(vals.k_cache), f32(vals.v_cache), wl.block_tables, kv_lens,
+                    wl.block_size, wl.softmax_scale)
+    return b, out, ref
+
+
+def test_decode_edge_lengths(pkv):
+    lens = [1, 2, 31, 32, 33, 255, 256, 257, 511, 512, 513, 1000, 4096, 0, 7, 0]
+    b, out, ref = _decode_only(pkv, lens, seed=11)
+    assert_attention_close(out, ref, "edge lengths")
+    assert torch.count_nonzero(out[13]).item() == 0 and torch.count_nonzero(out[15]).item() == 0
+    expect_no_device_error(pkv)
+
+
+def test_decode_nan_in_unused_slots_does_not_leak(pkv):
+    lens = [5, 300, 257, 1023, 64]
+    b, out, ref = _decode_only(pkv, lens, seed=12, poison=True)
+    assert_attention_close(out, ref, "poisoned pool")
+    expect_no_device_error(pkv)
+
+
+def test_decode_single_long_sequence_split_over_all_warps(pkv):
+    b, out, ref = _decode_only(pkv, [40960], seed=13)
+    assert_attention_close(out, ref, "one long sequence")
+    expect_no_device_error(pkv)
+
+
+def test_decode_many_short_sequences(pkv):
+    rng = np.random.default_rng(14)
+    lens = rng.integers(1, 70, size=600)
+    b, out, ref = _decode_only(pkv, lens, seed=14)
+    assert_attention_close(out, ref, "600 short sequences")
+    expect_no_device_error(pkv)
+
+
+def test_decode_deterministic_and_block_relabel_invariant(pkv):
+    wl = W.decode_b64(batch=16)
+    vals = W.paged_values(wl)
+    b = GpuBatch(wl, vals)
+    o1 = b.run_decode(pkv).clone()
+    o2 = b.run_decode(pkv).clone()
+    assert np.array_equal(bits(o1), bits(o2))
+    # move physical block i to pi[i]: the same logical data, other addresses
+    pi = np.random.default_rng(15).permutation(wl.num_blocks)
+    inv = torch.from_numpy(np.argsort(pi)).cuda()
+    k2 = b.k_cache[inv].contiguous()
+    v2 = b.v_cache[inv].contiguous()
+    bt2 = torch.from_numpy(np.where(wl.block_tables >= 0, pi[np.maximum(wl.block_tables, 0)], -1).astype(np.int32)).cuda()
+    o3 = pkv.pkv_decode(b.q, k2, v2, bt2, b.kv_lens, int(wl.kv_lens.max()), wl.softmax_scale)
+    assert np.array_equal(bits(o1), bits(o3))
+    expect_no_device_error(pkv)
+
+
+@pytest.mark.parametrize("name", ["decode-b8", "tiny-decode"])
+def test_decode_reuses_caller_workspace_and_out(pkv, name):
+    """Stale workspace contents must not matter, also when the grid has more warps than KV chunks."""
+    wl = W.decode_b64(batch=8) if name == "decode-b8" else W.tiny_decode()
+    b = GpuBatch(wl, W.paged_values(wl))
+    ws = pkv.decode_workspace(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim)
+    ws.fill_(0xAB)                       # contents need no initialisation
+    out = torch.full_like(b.q, float("nan"))
+    b.run_decode(pkv, out=out, workspace=ws)
+    assert_attention_close(out, b.oracle_decode(pools=(f32(b.cpu.k_cache), f32(b.cpu.v_cache))), "workspace reuse")
+    small = ws[: ws.numel() // 2]
+    with pytest.raises(pkv.PkvError) as e:
+        b.run_decode(pkv, workspace=small)
+    assert e.value.status == 3
+
+
+def test_decode_flags_block_id_outside_pool(pkv):
+    wl = W.decode_b64(batch=4)
+    b = GpuBatch(wl, W.paged_values(wl))
+    bt = b.block_tables.clone()
+    bt[1, 0] = wl.num_blocks + 5
+    pkv.pkv_decode(b.q, b.k_cache, b.v_cache, bt, b.kv_lens, int(wl.kv_lens.max()), wl.softmax_scale)
+    code, info = pkv.pkv_get_device_error(clear=True)
+    assert code == 1 and info == 1

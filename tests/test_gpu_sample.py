@@ -1,0 +1,88 @@
+"""a5 exponential-race sampler on the GPU against the oracle.
+
+The kernel decides the argmax in fp32 on the monotone form logits/T - ln e;
+the oracle evaluates the race literally in fp64.  Ids must be identical on
+every row whose oracle log-margin between the two best candidates exceeds
+NEAR_TIE (far above fp32 rounding of the key); on a near-tie row either of the
+oracle's two best candidates is accepted, and such rows are counted."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import sampler as sm
+
+pytestmark = pytest.mark.gpu
+
+NEAR_TIE = 1e-4
+
+
+def _check_ids(ids_gpu, logits, temps, seed, offset=0, max_near=2):
+    lg = logits.cpu().double().numpy()
+    T = temps.cpu().double().numpy()
+    e = sm.exponential_noise(seed, offset, range(lg.shape[0]), lg.shape[1])
+    ref, margin = sm.exponential_race(lg, T, e)
+    got = ids_gpu.cpu().numpy()
+    near = margin < NEAR_TIE
+    assert np.array_equal(got[~near], ref[~near]), np.nonzero(got[~near] != ref[~near])
+    for b in np.nonzero(near)[0]:
+        z = lg[b] / T[b]
+        r = np.exp(z - z.max()) / e[b]
+        top2 = np.argsort(r)[-2:]
+        assert got[b] in top2
+    assert near.sum() <= max_near
+    return int(near.sum())
+
+
+@pytest.mark.parametrize("vocab", [1000, 1001, 7])
+def test_sample_small_vs_oracle(pkv, vocab):
+    s = W.sampler_inputs(batch=96, vocab=vocab, seed=31, device="cpu")
+    ids = pkv.pkv_sample(s.logits.cuda(), s.temperatures.cuda(), s.seed, s.offset)
+    _check_ids(ids, s.logits, s.temperatures, s.seed, s.offset)
+    code, _ = pkv.pkv_get_device_error(clear=True)
+    assert code == 0
+
+
+def test_sample_full_vocab_vs_oracle(pkv):
+    s = W.sampler_inputs(batch=256, vocab=W.VOCAB_QWEN3, seed=1005, step=0, device="cpu")
+    ids = pkv.pkv_sample(s.logits.cuda(), s.temperatures.cuda(), s.seed, s.offset)
+    _check_ids(ids, s.logits, s.temperatures, s.seed, s.offset)
+
+
+def test_sample_row_offset_and_strided_rows(pkv):
+    s = W.sampler_inputs(batch=16, vocab=3000, seed=32, device="cpu")
+    wide = torch.zeros(16, 3100)
+    wide[:, :3000] = s.logits
+    view = wide.cuda()[:, :3000]
+    ids = pkv.pkv_sample(view, s.temperatures.cuda(), seed=77, offset=1000)
+    _check_ids(ids, s.logits, s.temperatures, 77, 1000)
+
+
+def test_sample_cold_temperature_is_argmax(pkv):
+    g = torch.Generator().manual_seed(33)
+    logits = torch.randn(64, 512, generator=g) * 3
+    temps = torch.full((64,), 1e-4)
+    ids = pkv.pkv_sample(logits.cuda(), temps.cuda(), seed=5)
+    top2 = torch.topk(logits, 2, dim=1).values
+    clear = (top2[:, 0] - top2[:, 1]) > 0.01
+    assert torch.equal(ids.cpu()[clear], logits.argmax(dim=1)[clear])
+
+
+def test_sample_invalid_temperature_flags_row(pkv):
+    logits = torch.randn(3, 100).cuda()
+    temps = torch.tensor([1.0, 0.0, 0.7]).cuda()
+    ids = pkv.pkv_sample(logits, temps, seed=1)
+    code, info = pkv.pkv_get_device_error(clear=True)
+    assert ids.cpu()[1].item() == -1 and code == 4 and info == 1
+    assert ids.cpu()[0].item() >= 0 and ids.cpu()[2].item() >= 0
+
+
+def test_sample_frequencies_follow_softmax(pkv):
+    """Many rows of one 4-token distribution: winner frequencies match p within 4 sigma."""
+    p = np.array([0.1, 0.2, 0.3, 0.4])
+    T = 0.7
+    n = 20000
+    logits = torch.from_numpy(np.log(p) * T).float().expand(n, 4).contiguous().cuda()
+    ids = pkv.pkv_sample(logits, torch.full((n,), T).cuda(), seed=99)
+    freq = np.bincount(ids.cpu().numpy(), minlength=4) / n
+    assert np.all(np.abs(freq - p) < 4 * np.sqrt(p * (1 - p) / n)), freq
