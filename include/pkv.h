@@ -192,6 +192,33 @@ PKV_API pkv_status pkv_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
                       pkv_stream_t stream);
 
 /*
+ * Decode without any allocation.  The paper has no counterpart: this is a
+ * library convenience for callers that cannot call cudaMalloc -- for example
+ * a plugin inside a host runtime that owns all device memory and hands it only
+ * its input and output buffers, or a service whose device-memory budget is
+ * fixed at start-up.
+ *
+ * Same arguments and result as pkv_decode, minus the workspace: the scratch
+ * is a PKV_DECODE_NOALLOC_SCRATCH_BYTES (4 MiB) array inside the library,
+ * which every GPU that loads the library holds until the process exits.  A
+ * batch whose pkv_decode_workspace_size() exceeds it returns
+ * PKV_ERR_UNSUPPORTED (it fits up to 427 sequences with 8 KV heads on a
+ * 152-SM GPU).
+ * The first call on each device looks up the array's device address; make
+ * that first call before any stream capture.  All calls share the array and
+ * it keeps the last call's contents (nothing in it needs to start at zero);
+ * calls that overlap on the GPU race on it and must be serialised.
+ */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+PKV_API pkv_status pkv_decode_noalloc(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                              const int32_t *block_tables, int32_t max_blocks_per_seq,
+                              const int32_t *context_lens, int32_t batch, int32_t max_context_len,
+                              int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t block_size, int32_t num_blocks, float softmax_scale,
+                              pkv_bf16 *out, pkv_stream_t stream);
+
+/*
  * a5. Temperature sampling by exponential race.
  * Visual atlas fig. 23: the engine samples with temperature only, as an
  * exponential race: winner = argmax_v p_v / e_v (= argmin e_v / p_v), with

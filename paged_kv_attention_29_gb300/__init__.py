@@ -30,7 +30,7 @@ __all__ = [
     "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
     "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
     "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error",
-    "decode_workspace", "DEVERR",
+    "decode_workspace", "pkv_decode_noalloc", "DEVERR",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +81,9 @@ def load() -> ctypes.CDLL:
         "pkv_decode": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
                                       _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_float, _c_ptr,
                                       _c_ptr, _c_size, _c_ptr]),
+        "pkv_decode_noalloc": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32,
+                                              _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
+                                              _c_float, _c_ptr, _c_ptr]),
         "pkv_sample": (ctypes.c_int, [_c_ptr, _c_int32, _c_int32, _c_int64, _c_ptr, _c_u64, _c_u64, _c_ptr,
                                       _c_ptr]),
         "pkv_get_device_error": (ctypes.c_int, [ctypes.POINTER(_c_int32), ctypes.POINTER(_c_int32), _c_int32]),
@@ -247,6 +250,28 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
                              _ptr(context_lens), batch, int(max_context_len), hq, hkv, d, bs, nb,
                              float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
            "pkv_decode")
+    return out
+
+
+def pkv_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                       context_lens: torch.Tensor, max_context_len: int, softmax_scale: float,
+                       out: torch.Tensor, stream=None) -> torch.Tensor:
+    """pkv_decode for callers that cannot allocate: the scratch lives inside the
+    library (4 MiB per GPU, shared by all calls, so overlapping calls race) and
+    ``out`` must be given.  A batch too large for that scratch raises PkvError."""
+    nb, bs, hkv, d = _pool_shape(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(q, "q", torch.bfloat16, 3)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    _check(out, "out", torch.bfloat16, 3)
+    batch, hq, dq = q.shape
+    if dq != d or context_lens.shape[0] != batch or block_tables.shape[0] != batch or out.shape != q.shape:
+        raise ValueError("q, out, context_lens and block_tables disagree")
+    _raise(load().pkv_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                     block_tables.shape[1], _ptr(context_lens), batch, int(max_context_len), hq,
+                                     hkv, d, bs, nb, float(softmax_scale), _ptr(out), _stream(stream)),
+           "pkv_decode_noalloc")
     return out
 
 
