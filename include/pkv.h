@@ -144,7 +144,11 @@ PKV_API pkv_status pkv_store_kvcache(const pkv_bf16 *k, const pkv_bf16 *v, int64
  *   out  bf16 [total_q, num_heads, head_dim] packed, written; rows of a
  *        sequence with q_len = 0 do not exist
  *   max_seqlen_q / max_seqlen_k  bounds on q_len / k_len (host-known)
- *   workspace  may be NULL when pkv_prefill_workspace_size() returns 0
+ *   softmax_scale  > 0
+ *   workspace  >= pkv_prefill_workspace_size(num_seqs, num_heads, num_kv_heads,
+ *        head_dim, max_seqlen_q) bytes: the work list, sorted by cost, that a
+ *        planning launch writes before the attention launch reads it; needs no
+ *        initialisation
  * Accumulation in fp32, probabilities rounded to bf16 for the PV product,
  * output rounded to bf16 once.
  */

@@ -207,7 +207,10 @@ def pkv_prefill_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
     if out is None:
         out = torch.empty_like(q)
     _check(out, "out", torch.bfloat16, 3)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if workspace is None:
+        n = pkv_prefill_workspace_size(num_seqs, hq, hkv, d, int(max_seqlen_q))
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
     _raise(load().pkv_prefill_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
                                      _ptr(block_tables), block_tables.shape[1], num_seqs, total_q, int(max_seqlen_q),
                                      int(max_seqlen_k), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),

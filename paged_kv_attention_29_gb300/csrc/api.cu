@@ -154,8 +154,9 @@ pkv_status pkv_store_kvcache(const pkv_bf16* k, const pkv_bf16* v, int64_t n_tok
 
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t max_seqlen_q) {
-    (void)num_seqs; (void)num_heads; (void)num_kv_heads; (void)head_dim; (void)max_seqlen_q;
-    return 0;
+    if (num_seqs < 0 || max_seqlen_q < 0 || !supported_shape(num_heads, num_kv_heads, head_dim, kBlockQuantum))
+        return 0;
+    return prefill_workspace_bytes(num_seqs, max_seqlen_q);
 }
 
 pkv_status pkv_prefill_varlen(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
@@ -166,9 +167,8 @@ pkv_status pkv_prefill_varlen(const pkv_bf16* q, const pkv_bf16* k_cache, const 
                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
                               float softmax_scale, pkv_bf16* out, void* workspace,
                               size_t workspace_bytes, pkv_stream_t stream) {
-    (void)workspace; (void)workspace_bytes;
     if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || max_blocks_per_seq <= 0 ||
-        num_blocks <= 0 || !(softmax_scale == softmax_scale))
+        num_blocks <= 0 || !(softmax_scale > 0.f) || softmax_scale == INFINITY)
         return PKV_ERR_INVALID_ARG;
     if (!supported_shape(num_heads, num_kv_heads, head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
     if (max_seqlen_q > max_seqlen_k) return PKV_ERR_INVALID_ARG;
@@ -199,6 +199,8 @@ pkv_status pkv_prefill_varlen(const pkv_bf16* q, const pkv_bf16* k_cache, const 
     a.block_size = block_size;
     a.num_blocks = num_blocks;
     a.softmax_scale = softmax_scale;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
     return launch_prefill(a, err, as_stream(stream));
 }
 

@@ -78,8 +78,11 @@ struct PrefillArgs {
     int block_size;
     int num_blocks;
     float softmax_scale;
+    void* workspace;
+    size_t workspace_bytes;
 };
 
+size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q);
 pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream);
 
 // ---- a5 ---------------------------------------------------------------------

@@ -6,24 +6,37 @@
 // of a chunk sees keys j <= i + k_len - q_len), fig. 18 (two query heads share
 // a K/V head), fig. 22 (blockwise evaluation without materialising scores).
 //
-// One CTA computes a 128-row tile: 64 query tokens x the 2 query heads that
-// share KV head g.  Packing both heads into the MMA's M dimension means both
-// read the same K/V tile, loaded once, with no cross-CTA traffic.
+// Work unit: 128 query tokens of one sequence x one KV head g, split into two
+// 128-row tiles A and B (64 tokens x the 2 query heads of the group each, so
+// both heads read one K/V tile).  Per unit and 128-key tile j:
 //
-//   Q tile   smem, two 128B-swizzled boxes (head dims 0-63, 64-127), rows in
-//            (token, head) order straight from the [tokens, heads, 128] layout
-//   K, V     128 keys (half of a 256-token block) per tile, two boxes each,
-//            double-buffered; cut from the pool by a 4-D tensor map at the
-//            physical block the block table names
-//   S = QK^T tcgen05.mma M=128 N=128 K=16 x 8, fp32 in TMEM (two buffers)
-//   P        bf16, written back to TMEM over its own S buffer; O += P V with P
-//            as the TMEM A operand and V as an MN-major smem B operand
-//   O        fp32 in TMEM; rescaled only when a row max grows by more than
-//            2^8 (the stale max keeps exp2 below 256, and O and l share it)
+//   S_X(j) = Q_X K_j^T      tcgen05.mma M=128 N=128, 8 x K=16, fp32 in TMEM
+//   P_X(j)                  masked online softmax by warpgroup X, bf16 over S_X
+//   O_X   += P_X(j) V_j     tcgen05.mma with P from TMEM (A operand), V MN-major
 //
-// Warp roles: warps 0-3 own TMEM lanes 0-127 (one row each: mask, online
-// softmax, O rescale, epilogue); warp 4 issues TMA; warp 5 allocates TMEM and
-// one of its lanes issues every MMA.
+// The MMA warp issues S_A(0) S_B(0) | PV_A(0) S_A(1) PV_B(0) S_B(1) | ... so
+// the tensor core works on one tile while the other tile's warpgroup runs its
+// softmax.  Because one commit tracks every earlier MMA, S_X(j) landing means
+// PV_X(j-1) landed, so a warpgroup may rescale O_X after it sees S_X(j) with
+// no further wait; O is rescaled only when a row max grows by more than 2^8
+// (P then stays below 256, and O and the row sum share the stale max).
+//
+// The softmax is the critical path, so it is written for the fewest issued
+// instructions per score: one 3-input max per two scores, the exponent
+// argument as one packed fp32x2 FMA per two scores, one special-function
+// exp2, a packed fp32x2 add for the row sum and one bf16x2 pack per two; the
+// mask is applied only on tiles the diagonal crosses.
+//
+// Persistent CTAs (one per SM) walk units in a static snake order over a list
+// that a one-CTA plan kernel sorts by cost (KV tiles) and leaves in the
+// workspace; the two launches are chained with programmatic dependent launch
+// so this kernel's set-up overlaps the plan.
+//
+// Warps 0-3: softmax of tile A (TMEM lanes 0-127), warps 4-7: tile B; warp 8:
+// TMA producer; warp 9: TMEM allocation and the single MMA-issuing thread;
+// warps 10-11 only complete the third warpgroup for the register split.
+#include <algorithm>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -32,38 +45,48 @@ namespace {
 
 constexpr int D = kHeadDim;
 constexpr int G = kGroup;
-constexpr int QTOK = 64;                  // query tokens per tile (x G heads = 128 rows)
+constexpr int QTOK = 64;                  // tokens per 128-row tile
+constexpr int UNIT_TOK = 2 * QTOK;        // tokens per unit (tiles A and B)
 constexpr int ROWS = QTOK * G;            // MMA M
-constexpr int KT = 128;                   // keys per KV tile (MMA N of QK^T)
+constexpr int KT = 128;                   // keys per KV tile
 constexpr int HALF_BYTES = ROWS * 64 * 2; // one 128B-swizzled box: 128 rows x 64 dims = 16 KiB
 constexpr int TILE_BYTES = 2 * HALF_BYTES;
-constexpr int THREADS = 192;
+constexpr int THREADS = 384;              // 3 warpgroups: softmax A, softmax B, producer + MMA
+constexpr int PRODUCER_WARP = 8, MMA_WARP = 9;
+// setmaxnreg split: the softmax warpgroups keep a 128-column fp32 S row per
+// thread; the control warpgroup needs few.  2*128*208 + 128*80 = 63488
+// registers, within the 384 x 168 that the launch must provide (checked on
+// the host before every launch).
+constexpr uint32_t kSoftmaxRegs = 208, kControlRegs = 80, kMinLaunchRegs = 168;
 constexpr int TMEM_COLS = 512;
-constexpr int S_COL0 = 0, S_COL1 = 128, O_COL = 256;
+__host__ __device__ constexpr uint32_t S_COL(int x) { return 128u * x; }         // S / P of tile x
+__host__ __device__ constexpr uint32_t O_COL(int x) { return 256u + 128u * x; }  // O of tile x
 constexpr float kRescaleLog2 = 8.0f;
 
-// shared-memory layout (offsets from the 1024-aligned base)
-constexpr int SM_Q = 0;
-constexpr int SM_K = SM_Q + TILE_BYTES;           // 2 stages
+// shared memory (offsets from the 1024-aligned base)
+constexpr int SM_QA = 0;
+constexpr int SM_QB = SM_QA + TILE_BYTES;
+constexpr int SM_K = SM_QB + TILE_BYTES;          // 2 stages
 constexpr int SM_V = SM_K + 2 * TILE_BYTES;       // 2 stages
 constexpr int SM_BAR = SM_V + 2 * TILE_BYTES;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done,
-// o_final (the last PV landed), drain (every MMA landed)
-constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 3, BAR_VF = 5, BAR_VE = 7, BAR_SF = 9, BAR_PF = 11,
-              BAR_PV = 13, BAR_OFIN = 14, BAR_DRAIN = 15, NUM_BARS = 16;
-constexpr int SM_MISC = SM_BAR + NUM_BARS * 8;   // tmem base (u32), abort flag (u32)
-constexpr int SMEM_BYTES = SM_MISC + 16 + 1024;  // + alignment slack
+enum {
+    BAR_QF = 0, BAR_QE, BAR_KF, BAR_KF1, BAR_KE, BAR_KE1, BAR_VF, BAR_VF1, BAR_VE, BAR_VE1,
+    BAR_SF, BAR_SF1, BAR_PF, BAR_PF1, BAR_OF, BAR_OF1, BAR_OE, BAR_OE1, BAR_DRAIN, NUM_BARS
+};
+constexpr int SM_MISC = SM_BAR + NUM_BARS * 8;    // [0] TMEM base, [1] abort flag
+constexpr int SMEM_BYTES = SM_MISC + 16 + 1024;
 
 struct Params {
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* block_tables;
+    const uint32_t* plan;     // [0] = number of (seq, pair) entries, then entries (seq << 16 | pair)
     uint16_t* out;
     int max_blocks;
     int num_heads;
+    int num_kv_heads;
     int block_size;
     int num_blocks;
-    int n_qtiles;
     float scale_log2;
     int* err;
 };
@@ -71,11 +94,10 @@ struct Params {
 struct Ctl {
     volatile uint32_t* abort;
     int* err;
-    int where;
 };
 
-// Wait for a phase; any role's timeout aborts the whole CTA.
-__device__ __noinline__ bool wait_phase(const Ctl& c, uint32_t bar, uint32_t parity) {
+// Inlined on purpose: a call inside a setmaxnreg region cannot be register-allocated.
+__device__ __forceinline__ bool wait_phase(const Ctl& c, uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
@@ -84,229 +106,366 @@ __device__ __noinline__ bool wait_phase(const Ctl& c, uint32_t bar, uint32_t par
         if (*c.abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *c.abort = 1u;
-            record_error(c.err, PKV_DEVERR_TIMEOUT, c.where);
+            record_error(c.err, PKV_DEVERR_TIMEOUT, static_cast<int>(blockIdx.x));
             return false;
         }
     }
 }
 
-// Wait used while draining after an abort: bounded, ignores the abort flag.
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity))
         if (global_ns() - t0 > kWaitLimitNs) return false;
     return true;
 }
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) {
-    // 128B swizzle, K-major: rows of 128 B, 8-row atoms 1024 B apart (LBO unused)
-    return smem_desc(addr, 16, 1024, 2);
-}
-__device__ __forceinline__ uint64_t vmajor_desc(uint32_t addr) {
-    // 128B swizzle, MN-major (V as [keys][dims]): the second 64-dim box is
-    // HALF_BYTES further (LBO), 8-key groups are 1024 B apart (SBO)
-    return smem_desc(addr, HALF_BYTES, 1024, 2);
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) { return smem_desc(addr, 16, 1024, 2); }
+__device__ __forceinline__ uint64_t vmajor_desc(uint32_t addr) { return smem_desc(addr, HALF_BYTES, 1024, 2); }
+
+// KV tiles a 64-token query tile needs: keys up to its last token's position.
+__device__ __forceinline__ int kv_tiles(int first_tok, int ql, int offset) {
+    if (first_tok >= ql) return 0;
+    const int last = min(first_tok + QTOK, ql) - 1;
+    return (last + offset + KT) / KT;     // ceil((last + offset + 1) / KT)
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
-prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    const int seq = blockIdx.z;
-    const int g = blockIdx.y;
-    const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);   // heavier tiles first
-    const int q_start = __ldg(p.cu_q + seq);
-    const int ql = __ldg(p.cu_q + seq + 1) - q_start;
-    const int kl = __ldg(p.cu_k + seq + 1) - __ldg(p.cu_k + seq);
-    if (qt * QTOK >= ql) return;
-    if (ql > kl || kl > p.max_blocks * p.block_size) {
-        if (threadIdx.x == 0) record_error(p.err, PKV_DEVERR_SEQLENS, seq);
-        return;
+struct Unit {
+    int seq, pair, g;
+    int q_start, ql, kl, offset;
+    int n[2];          // KV tiles of tile A and tile B (B may be 0)
+};
+
+__device__ __forceinline__ Unit unit_at(const Params& p, int idx) {
+    Unit u;
+    const uint32_t e = __ldg(p.plan + 1 + idx / p.num_kv_heads);
+    u.g = idx % p.num_kv_heads;
+    u.seq = static_cast<int>(e >> 16);
+    u.pair = static_cast<int>(e & 0xffffu);
+    u.q_start = __ldg(p.cu_q + u.seq);
+    u.ql = __ldg(p.cu_q + u.seq + 1) - u.q_start;
+    const int k0 = __ldg(p.cu_k + u.seq);
+    u.kl = __ldg(p.cu_k + u.seq + 1) - k0;
+    u.offset = u.kl - u.ql;
+    u.n[0] = kv_tiles(u.pair * UNIT_TOK, u.ql, u.offset);
+    u.n[1] = kv_tiles(u.pair * UNIT_TOK + QTOK, u.ql, u.offset);
+    return u;
+}
+
+// Index of this CTA's r-th unit in the cost-sorted list (snake order), or -1.
+__device__ __forceinline__ int unit_index(int r, int total) {
+    const int G_ = static_cast<int>(gridDim.x);
+    const int c = static_cast<int>(blockIdx.x);
+    const int idx = r * G_ + ((r & 1) ? (G_ - 1 - c) : c);
+    return idx < total ? idx : -1;
+}
+
+// -------------------------------------------------------------------------
+// plan: (seq, pair) entries sorted by cost, most KV tiles first
+// -------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q,
+                                                           const int32_t* __restrict__ cu_k, int num_seqs,
+                                                           int max_blocks, int block_size, int max_cost,
+                                                           uint32_t* __restrict__ plan, int* err) {
+    extern __shared__ int hist[];          // [max_cost + 1]
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = threadIdx.x; i <= max_cost; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    auto seq_ok = [&](int s, int& ql, int& kl) {
+        ql = cu_q[s + 1] - cu_q[s];
+        kl = cu_k[s + 1] - cu_k[s];
+        return ql >= 0 && ql <= kl && kl <= max_blocks * block_size;
+    };
+    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+        int ql, kl;
+        if (!seq_ok(s, ql, kl)) {
+            record_error(err, PKV_DEVERR_SEQLENS, s);
+            continue;
+        }
+        const int off = kl - ql;
+        for (int pr = 0; pr * UNIT_TOK < ql; ++pr) {
+            const int cost = min(max_cost, kv_tiles(pr * UNIT_TOK, ql, off) + kv_tiles(pr * UNIT_TOK + QTOK, ql, off));
+            atomicAdd(&hist[cost], 1);
+        }
     }
-    const int offset = kl - ql;
-    const int last_q = min(qt * QTOK + QTOK, ql) - 1;
-    const int keys_needed = last_q + offset + 1;              // <= kl
-    const int n_kv = (keys_needed + KT - 1) / KT;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int c = max_cost; c >= 0; --c) { const int x = hist[c]; hist[c] = run; run += x; }
+        plan[0] = static_cast<uint32_t>(run);
+    }
+    __syncthreads();
+    for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
+        int ql, kl;
+        if (!seq_ok(s, ql, kl)) continue;
+        const int off = kl - ql;
+        for (int pr = 0; pr * UNIT_TOK < ql; ++pr) {
+            const int cost = min(max_cost, kv_tiles(pr * UNIT_TOK, ql, off) + kv_tiles(pr * UNIT_TOK + QTOK, ql, off));
+            const int pos = atomicAdd(&hist[cost], 1);
+            plan[1 + pos] = (static_cast<uint32_t>(s) << 16) | static_cast<uint32_t>(pr);
+        }
+    }
+}
 
+// -------------------------------------------------------------------------
+// main kernel
+// -------------------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS, 1)
+prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t sQ = base + SM_Q, sK = base + SM_K, sV = base + SM_V;
+    const uint32_t sQ[2] = {base + SM_QA, base + SM_QB};
+    const uint32_t sK = base + SM_K, sV = base + SM_V;
     const uint32_t bars = base + SM_BAR;
     auto bar = [&](int i) { return bars + 8u * i; };
     uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + SM_MISC);
-    Ctl ctl{reinterpret_cast<volatile uint32_t*>(misc + 1), p.err, seq};
+    Ctl ctl{reinterpret_cast<volatile uint32_t*>(misc + 1), p.err};
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
     if (tid == 0) {
-        mbar_init(bar(BAR_Q), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(BAR_KF + s), 1);
-            mbar_init(bar(BAR_KE + s), 1);
-            mbar_init(bar(BAR_VF + s), 1);
-            mbar_init(bar(BAR_VE + s), 1);
-            mbar_init(bar(BAR_SF + s), 1);
-            mbar_init(bar(BAR_PF + s), ROWS);
+        for (int i = 0; i < NUM_BARS; ++i) {
+            const bool softmax_arrive = (i == BAR_PF || i == BAR_PF1 || i == BAR_OE || i == BAR_OE1);
+            mbar_init(bar(i), softmax_arrive ? ROWS : 1);
         }
-        mbar_init(bar(BAR_PV), 1);
-        mbar_init(bar(BAR_OFIN), 1);
-        mbar_init(bar(BAR_DRAIN), 1);
         misc[1] = 0u;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == MMA_WARP) {
         tmem_alloc(base + SM_MISC, TMEM_COLS);
         tmem_relinquish();
+    }
+    if (warp == PRODUCER_WARP && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
+    // everything above overlaps the plan kernel; global reads start here
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int total_units = static_cast<int>(__ldg(p.plan)) * p.num_kv_heads;
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
+    // Each warpgroup runs its own branch to the kernel's end (no common tail, so
+    // every instruction has one register budget); every branch ends at the same
+    // CTA barrier, after which the MMA warp releases TMEM.
+    if (warp == PRODUCER_WARP) {
+        regs_dec<kControlRegs>();
+        // ---------------------------------------------------------------- TMA
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            const int qrow = q_start + qt * QTOK;
-            mbar_arrive_expect_tx(bar(BAR_Q), TILE_BYTES);
-            tma_load_3d(sQ, &tm_q, bar(BAR_Q), 0, G * g, qrow);
-            tma_load_3d(sQ + HALF_BYTES, &tm_q, bar(BAR_Q), 64, G * g, qrow);
-            const int32_t* bt = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks;
-            int issued_k = 0, issued_v = 0;
-            bool ok = true;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j & 1;
-                const int key0 = j * KT;
-                const int lb = key0 / p.block_size;
-                const int phys = __ldg(bt + lb);
-                if (phys < 0 || phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, seq);
-                const int off = key0 - lb * p.block_size;
-                if (j >= 2 && !(ok = wait_phase(ctl, bar(BAR_KE + st), ((j - 2) >> 1) & 1))) break;
-                mbar_arrive_expect_tx(bar(BAR_KF + st), TILE_BYTES);
-                tma_load_4d(sK + st * TILE_BYTES, &tm_k, bar(BAR_KF + st), 0, g, off, phys);
-                tma_load_4d(sK + st * TILE_BYTES + HALF_BYTES, &tm_k, bar(BAR_KF + st), 64, g, off, phys);
-                ++issued_k;
-                if (j >= 2 && !(ok = wait_phase(ctl, bar(BAR_VE + st), ((j - 2) >> 1) & 1))) break;
-                mbar_arrive_expect_tx(bar(BAR_VF + st), TILE_BYTES);
-                tma_load_4d(sV + st * TILE_BYTES, &tm_v, bar(BAR_VF + st), 0, g, off, phys);
-                tma_load_4d(sV + st * TILE_BYTES + HALF_BYTES, &tm_v, bar(BAR_VF + st), 64, g, off, phys);
-                ++issued_v;
+            int t = 0;           // KV tiles issued by this CTA
+            int issued_k = 0, issued_v = 0, uq = 0;
+            for (int r = 0;; ++r) {
+                const int idx = unit_index(r, total_units);
+                if (idx < 0) break;
+                const Unit u = unit_at(p, idx);
+                const int n = max(u.n[0], u.n[1]);
+                if (uq >= 1 && !wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1)) break;
+                const int qrow = u.q_start + u.pair * UNIT_TOK;
+                mbar_arrive_expect_tx(bar(BAR_QF), u.n[1] > 0 ? 2 * TILE_BYTES : TILE_BYTES);
+                tma_load_3d(sQ[0], &tm_q, bar(BAR_QF), 0, G * u.g, qrow);
+                tma_load_3d(sQ[0] + HALF_BYTES, &tm_q, bar(BAR_QF), 64, G * u.g, qrow);
+                if (u.n[1] > 0) {
+                    tma_load_3d(sQ[1], &tm_q, bar(BAR_QF), 0, G * u.g, qrow + QTOK);
+                    tma_load_3d(sQ[1] + HALF_BYTES, &tm_q, bar(BAR_QF), 64, G * u.g, qrow + QTOK);
+                }
+                ++uq;
+                const int32_t* bt = p.block_tables + static_cast<int64_t>(u.seq) * p.max_blocks;
+                bool ok = true;
+                for (int j = 0; j < n; ++j, ++t) {
+                    const int st = t & 1;
+                    const int key0 = j * KT;
+                    const int lb = key0 / p.block_size;
+                    const int phys = __ldg(bt + lb);
+                    if (phys < 0 || phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, u.seq);
+                    const int off = key0 - lb * p.block_size;
+                    if (t >= 2 && !(ok = wait_phase(ctl, bar(BAR_KE + st), ((t >> 1) - 1) & 1))) break;
+                    mbar_arrive_expect_tx(bar(BAR_KF + st), TILE_BYTES);
+                    tma_load_4d(sK + st * TILE_BYTES, &tm_k, bar(BAR_KF + st), 0, u.g, off, phys);
+                    tma_load_4d(sK + st * TILE_BYTES + HALF_BYTES, &tm_k, bar(BAR_KF + st), 64, u.g, off, phys);
+                    ++issued_k;
+                    if (t >= 2 && !(ok = wait_phase(ctl, bar(BAR_VE + st), ((t >> 1) - 1) & 1))) break;
+                    mbar_arrive_expect_tx(bar(BAR_VF + st), TILE_BYTES);
+                    tma_load_4d(sV + st * TILE_BYTES, &tm_v, bar(BAR_VF + st), 0, u.g, off, phys);
+                    tma_load_4d(sV + st * TILE_BYTES + HALF_BYTES, &tm_v, bar(BAR_VF + st), 64, u.g, off, phys);
+                    ++issued_v;
+                }
+                if (!ok) break;
             }
             if (*ctl.abort) {
-                // let every copy already issued land before shared memory is released
-                wait_drain(bar(BAR_Q), 0);
-                for (int j = max(0, issued_k - 2); j < issued_k; ++j) wait_drain(bar(BAR_KF + (j & 1)), (j >> 1) & 1);
-                for (int j = max(0, issued_v - 2); j < issued_v; ++j) wait_drain(bar(BAR_VF + (j & 1)), (j >> 1) & 1);
+                // copies already issued must land before shared memory is released
+                if (uq > 0) wait_drain(bar(BAR_QF), (uq - 1) & 1);
+                for (int k = max(0, issued_k - 2); k < issued_k; ++k) wait_drain(bar(BAR_KF + (k & 1)), (k >> 1) & 1);
+                for (int k = max(0, issued_v - 2); k < issued_v; ++k) wait_drain(bar(BAR_VF + (k & 1)), (k >> 1) & 1);
             }
         }
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+    } else if (warp == MMA_WARP) {
+        regs_dec<kControlRegs>();
+        // ---------------------------------------------------------------- MMA
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(ROWS, KT, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(ROWS, D, 0, 1);
-            bool ok = wait_phase(ctl, bar(BAR_Q), 0);
-            auto issue_pv = [&](int jj) -> bool {
-                const int st = jj & 1;
-                if (!wait_phase(ctl, bar(BAR_PF + st), (jj >> 1) & 1)) return false;
-                if (!wait_phase(ctl, bar(BAR_VF + st), (jj >> 1) & 1)) return false;
-                tc_fence_after();
-                const int keys_here = min(KT, kl - jj * KT);
-                const int ksteps = (keys_here + 15) >> 4;
-                const int tail = keys_here & 15;
-                if (tail) {
-                    // rows past the sequence's last key may hold anything (freed blocks are
-                    // not cleared); P is zero there but 0 * NaN is NaN, so clear them
-                    uint8_t* vt = gbase + SM_V + st * TILE_BYTES;
-                    for (int r = keys_here; r < ksteps * 16; ++r) {
-                        uint4* r0 = reinterpret_cast<uint4*>(vt + r * 128);
-                        uint4* r1 = reinterpret_cast<uint4*>(vt + HALF_BYTES + r * 128);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) { r0[c] = make_uint4(0, 0, 0, 0); r1[c] = make_uint4(0, 0, 0, 0); }
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                const uint32_t p_tmem = tmem + (st ? S_COL1 : S_COL0);
-                const uint32_t vbase = sV + st * TILE_BYTES;
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    mma_ts(tmem + O_COL, p_tmem + ks * 8, vmajor_desc(vbase + ks * 16 * 128), idesc_pv,
-                           (jj > 0 || ks > 0) ? 1u : 0u);
-                }
-                mma_commit(bar(BAR_PV));
-                mma_commit(bar(BAR_VE + st));
-                return true;
-            };
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int st = j & 1;
-                if (!(ok = wait_phase(ctl, bar(BAR_KF + st), (j >> 1) & 1))) break;
-                tc_fence_after();
+            int t = 0, uq = 0;
+            int cntP[2] = {0, 0}, uact[2] = {0, 0};
+            bool ok = true;
+            int s_left = 0;      // S MMAs of the current unit not yet issued
+            auto issue_s = [&](int X, int st) {
                 const uint32_t kbase = sK + st * TILE_BYTES;
-                const uint32_t s_tmem = tmem + (st ? S_COL1 : S_COL0);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t koff = (ks >> 2) * HALF_BYTES + (ks & 3) * 32;
-                    mma_ss(s_tmem, kmajor_desc(sQ + koff), kmajor_desc(kbase + koff), idesc_qk, ks > 0 ? 1u : 0u);
+                    mma_ss(tmem + S_COL(X), kmajor_desc(sQ[X] + koff), kmajor_desc(kbase + koff), idesc_qk,
+                           ks > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(BAR_SF + st));
-                mma_commit(bar(BAR_KE + st));
-                if (j >= 1 && !(ok = issue_pv(j - 1))) break;
+                mma_commit(bar(BAR_SF + X));
+                if (--s_left == 0) mma_commit(bar(BAR_QE));   // the unit's Q tiles are no longer read
+            };
+            for (int r = 0; ok; ++r) {
+                const int idx = unit_index(r, total_units);
+                if (idx < 0) break;
+                const Unit u = unit_at(p, idx);
+                const int n = max(u.n[0], u.n[1]);
+                s_left = u.n[0] + u.n[1];
+                if (!(ok = wait_phase(ctl, bar(BAR_QF), uq & 1))) break;
+                ++uq;
+                if (!(ok = wait_phase(ctl, bar(BAR_KF + (t & 1)), (t >> 1) & 1))) break;
+                tc_fence_after();
+                issue_s(0, t & 1);
+                if (u.n[1] > 0) issue_s(1, t & 1);
+                mma_commit(bar(BAR_KE + (t & 1)));
+                for (int j = 0; j < n && ok; ++j) {
+                    const int tj = t + j;
+                    const int st = tj & 1;
+                    bool v_ready = false, k_next_ready = false, v_tail_done = false;
+                    const int keys_here = min(KT, u.kl - j * KT);
+                    const int ksteps = (keys_here + 15) >> 4;
+#pragma unroll
+                    for (int X = 0; X < 2; ++X) {
+                        if (!ok) break;
+                        if (j < u.n[X]) {
+                            if (!(ok = wait_phase(ctl, bar(BAR_PF + X), cntP[X] & 1))) break;
+                            ++cntP[X];
+                            if (!v_ready) {
+                                if (!(ok = wait_phase(ctl, bar(BAR_VF + st), (tj >> 1) & 1))) break;
+                                v_ready = true;
+                            }
+                            if (j == 0 && uact[X] >= 1 && !(ok = wait_phase(ctl, bar(BAR_OE + X), (uact[X] - 1) & 1)))
+                                break;
+                            tc_fence_after();
+                            if ((keys_here & 15) && !v_tail_done) {
+                                // rows past the sequence's last key may hold anything (freed blocks are not
+                                // cleared); their P is zero but 0 * NaN is NaN, so clear them
+                                uint8_t* vt = gbase + SM_V + st * TILE_BYTES;
+                                for (int rr = keys_here; rr < ksteps * 16; ++rr) {
+                                    uint4* r0 = reinterpret_cast<uint4*>(vt + rr * 128);
+                                    uint4* r1 = reinterpret_cast<uint4*>(vt + HALF_BYTES + rr * 128);
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c) {
+                                        r0[c] = make_uint4(0, 0, 0, 0);
+                                        r1[c] = make_uint4(0, 0, 0, 0);
+                                    }
+                                }
+                                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                                v_tail_done = true;
+                            }
+                            const uint32_t vbase = sV + st * TILE_BYTES;
+                            for (int ks = 0; ks < ksteps; ++ks)
+                                mma_ts(tmem + O_COL(X), tmem + S_COL(X) + ks * 8, vmajor_desc(vbase + ks * 16 * 128),
+                                       idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+                            if (j == u.n[X] - 1) {
+                                mma_commit(bar(BAR_OF + X));
+                                ++uact[X];
+                            }
+                        }
+                        if (j + 1 < u.n[X]) {
+                            if (!k_next_ready) {
+                                if (!(ok = wait_phase(ctl, bar(BAR_KF + ((tj + 1) & 1)), ((tj + 1) >> 1) & 1))) break;
+                                tc_fence_after();
+                                k_next_ready = true;
+                            }
+                            issue_s(X, (tj + 1) & 1);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(BAR_VE + st));
+                    if (j + 1 < n) mma_commit(bar(BAR_KE + ((tj + 1) & 1)));
+                }
+                t += n;
             }
-            if (ok) ok = issue_pv(n_kv - 1);
-            if (ok) mma_commit(bar(BAR_OFIN));
-            // everything issued has to finish before TMEM is released
             mma_commit(bar(BAR_DRAIN));
             wait_drain(bar(BAR_DRAIN), 0);
         }
-    } else {
-        // ------------------------------------------------------------ softmax rows
-        const int row = tid;                       // TMEM lane
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    } else if (warp < 8) {
+        regs_inc<kSoftmaxRegs>();
+        // ---------------------------------------------------------------- softmax, tile X
+        const int X = warp >> 2;                  // 0: warps 0-3, 1: warps 4-7
+        const int row = tid & 127;                // TMEM lane
         const int ti = row >> 1;
         const int hh = row & 1;
-        const int qi = qt * QTOK + ti;
-        const bool row_valid = qi < ql;
-        const int jmax = min(qi + offset, kl - 1);   // last visible key
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        float m_used = -INFINITY, l = 0.f;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_off + S_COL(X);
+        const uint32_t o_tmem = tmem + lane_off + O_COL(X);
+        const float sc = p.scale_log2;
+        int cntS = 0, uact = 0;
         bool ok = true;
-        for (int j = 0; j < n_kv; ++j) {
-            const int st = j & 1;
-            ok = __all_sync(0xffffffffu, wait_phase(ctl, bar(BAR_SF + st), (j >> 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_off + (st ? S_COL1 : S_COL0);
-            uint32_t s[4][32];
+        for (int r = 0; ok; ++r) {
+            const int idx = unit_index(r, total_units);
+            if (idx < 0) break;
+            const Unit u = unit_at(p, idx);
+            const int nx = X ? u.n[1] : u.n[0];
+            if (nx == 0) continue;
+            const int qi = u.pair * UNIT_TOK + X * QTOK + ti;
+            const bool row_valid = qi < u.ql;
+            const int jmax = min(qi + u.offset, u.kl - 1);
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < nx; ++j) {
+                ok = __all_sync(0xffffffffu, wait_phase(ctl, bar(BAR_SF + X), cntS & 1));
+                if (!ok) break;
+                ++cntS;
+                tc_fence_after();
+                uint32_t sr[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + 32 * c, s[c]);
-            tmem_ld_wait();
-            const int lim = jmax - j * KT;         // columns <= lim are visible
-            float mt = -INFINITY;
+                for (int c = 0; c < 4; ++c) tmem_ld32(s_tmem + 32 * c, sr[c]);
+                tmem_ld_wait();
+                float s[128];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int e = 0; e < 128; ++e) s[e] = __uint_as_float(sr[e >> 5][e & 31]);
+                const int lim = jmax - j * KT;    // columns <= lim are visible
+                if (!__all_sync(0xffffffffu, lim >= KT - 1)) {
+                    // the diagonal crosses this tile (or the keys end in it): hide what the row may not see
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float x = (32 * c + e <= lim) ? __uint_as_float(s[c][e]) * p.scale_log2 : -INFINITY;
-                    s[c][e] = __float_as_uint(x);
-                    mt = fmaxf(mt, x);
+                    for (int e = 0; e < 128; ++e) s[e] = (e <= lim) ? s[e] : -INFINITY;
                 }
-            const float m_new = fmaxf(m_used, mt);
-            if (j == 0) {
-                m_used = m_new;
-            } else {
-                const bool need = m_new > m_used + kRescaleLog2;
-                if (__any_sync(0xffffffffu, need)) {
-                    // O holds sum_{k<j} P_k V_k scaled by 2^-m_used; PV_{j-1} must have landed.
-                    // S_j landing implies PV_{j-2} landed (one commit tracks all earlier MMAs),
-                    // so the phase parity of PV_{j-1} cannot alias.
-                    ok = __all_sync(0xffffffffu, wait_phase(ctl, bar(BAR_PV), (j - 1) & 1));
-                    if (!ok) break;
-                    tc_fence_after();
+                // row max of the raw scores (the scale is > 0), four independent 3-input chains
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 128; e += 8) {
+                    mx0 = fmax3(mx0, s[e + 0], s[e + 1]);
+                    mx1 = fmax3(mx1, s[e + 2], s[e + 3]);
+                    mx2 = fmax3(mx2, s[e + 4], s[e + 5]);
+                    mx3 = fmax3(mx3, s[e + 6], s[e + 7]);
+                }
+                const float m_new = fmax3(fmaxf(mx0, mx1), mx2, mx3) * sc;
+                if (j == 0) {
+                    m_used = m_new;
+                } else if (__any_sync(0xffffffffu, m_new > m_used + kRescaleLog2)) {
+                    // S_X(j) landed, so PV_X(j-1) has too: O_X is stable until P_X(j) is released
                     const float m_tgt = fmaxf(m_used, m_new);
-                    const float alpha = exp2f(m_used - m_tgt);
-                    const uint32_t o_tmem = tmem + lane_off + O_COL;
+                    const float alpha = ex2_ftz(m_used - m_tgt);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
@@ -320,33 +479,40 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     l *= alpha;
                     m_used = m_tgt;
                 }
-            }
-            // P = 2^(x - m_used) in bf16, over this tile's S buffer
-            uint32_t pk[2][32];
-            float rs = 0.f;
+                // P = 2^(s*scale - m_used) as bf16 pairs over the first 64 columns of this S buffer
+                // (all of S is already in registers, so nothing is overwritten before it is read)
+                const float neg_m = -m_used;
+                float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float p0 = exp2f(__uint_as_float(s[c][e]) - m_used);
-                    const float p1 = exp2f(__uint_as_float(s[c][e + 1]) - m_used);
-                    rs += p0 + p1;
-                    pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 32; e += 4) {
+                        const int b = 32 * c + e;
+                        float a0, a1, a2, a3;
+                        ffma2(a0, a1, s[b], s[b + 1], sc, sc, neg_m, neg_m);
+                        ffma2(a2, a3, s[b + 2], s[b + 3], sc, sc, neg_m, neg_m);
+                        const float p0 = ex2_ftz(a0), p1 = ex2_ftz(a1), p2 = ex2_ftz(a2), p3 = ex2_ftz(a3);
+                        fadd2(r0, r1, r0, r1, p0, p1);
+                        fadd2(r2, r3, r2, r3, p2, p3);
+                        pk[e >> 1] = pack_bf16x2(p0, p1);
+                        pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
+                    }
+                    tmem_st16(s_tmem + 16 * c, pk);
                 }
-            l += rs;
-            tmem_st32(s_tmem, pk[0]);
-            tmem_st32(s_tmem + 32, pk[1]);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar(BAR_PF + st));
-        }
-        // epilogue: O / l -> bf16
-        if (ok) ok = __all_sync(0xffffffffu, wait_phase(ctl, bar(BAR_OFIN), 0));
-        if (ok) {
+                l += (r0 + r1) + (r2 + r3);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(bar(BAR_PF + X));
+            }
+            if (!ok) break;
+            // epilogue: O_X / l -> bf16
+            ok = __all_sync(0xffffffffu, wait_phase(ctl, bar(BAR_OF + X), uact & 1));
+            if (!ok) break;
+            ++uact;
             tc_fence_after();
-            const uint32_t o_tmem = tmem + lane_off + O_COL;
             const float inv = 1.f / l;
-            uint16_t* dst = p.out + (static_cast<int64_t>(q_start + qi) * p.num_heads + G * g + hh) * D;
+            uint16_t* dst = p.out + (static_cast<int64_t>(u.q_start + qi) * p.num_heads + G * u.g + hh) * D;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t o[32];
@@ -365,20 +531,31 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(bar(BAR_OE + X));
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 5) {
-        tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tc_fence_before();
+        __syncthreads();
+    } else {
+        regs_dec<kControlRegs>();      // warps 10-11: complete the third warpgroup
+        __syncthreads();
     }
 }
 
+constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 }  // namespace
+
+size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q) {
+    const size_t pairs = static_cast<size_t>(num_seqs) * ((max_seqlen_q + UNIT_TOK - 1) / UNIT_TOK);
+    return align256((pairs + 1) * 4);
+}
 
 pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     if (a.num_seqs == 0 || a.total_q == 0 || a.max_seqlen_q == 0) return PKV_OK;
+    if (a.max_seqlen_q > 0xffff * UNIT_TOK) return PKV_ERR_UNSUPPORTED;
+    const size_t need = prefill_workspace_bytes(a.num_seqs, a.max_seqlen_q);
+    if (a.workspace == nullptr || a.workspace_bytes < need) return PKV_ERR_WORKSPACE;
     CUtensorMap tm_q, tm_k, tm_v;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_heads),
@@ -402,16 +579,20 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
                          strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return PKV_ERR_INVALID_ARG;
     }
+    const int max_cost = 2 * ((a.max_seqlen_k + KT - 1) / KT);
+    const size_t plan_smem = static_cast<size_t>(max_cost + 1) * 4;
+    if (plan_smem > 200 * 1024) return PKV_ERR_UNSUPPORTED;
     Params p;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
     p.block_tables = a.block_tables;
+    p.plan = static_cast<const uint32_t*>(a.workspace);
     p.out = a.out;
     p.max_blocks = a.max_blocks;
     p.num_heads = a.num_heads;
+    p.num_kv_heads = a.num_kv_heads;
     p.block_size = a.block_size;
     p.num_blocks = a.num_blocks;
-    p.n_qtiles = (a.max_seqlen_q + QTOK - 1) / QTOK;
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
     p.err = err;
 
@@ -419,14 +600,36 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        if (cudaFuncSetAttribute(prefill_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(prefill_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
+                cudaSuccess)
             return PKV_ERR_CUDA;
+        // the setmaxnreg split inside the kernel needs this many registers per thread at launch
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, prefill_fa_kernel) != cudaSuccess) return PKV_ERR_CUDA;
+        if (fa.numRegs < static_cast<int>(kMinLaunchRegs)) return PKV_ERR_UNSUPPORTED;
         configured_device = dev;
     }
-    dim3 grid(p.n_qtiles, a.num_kv_heads, a.num_seqs);
-    prefill_tcgen05_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tm_q, tm_k, tm_v, p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    prefill_plan_kernel<<<1, 1024, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.max_blocks, a.block_size,
+                                                        max_cost, static_cast<uint32_t*>(a.workspace), err);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+
+    const int64_t max_units = static_cast<int64_t>(a.num_seqs) *
+                              ((a.max_seqlen_q + UNIT_TOK - 1) / UNIT_TOK) * a.num_kv_heads;
+    const int grid = static_cast<int>(std::min<int64_t>(sm_count(), max_units));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, prefill_fa_kernel, tm_q, tm_k, tm_v, p) != cudaSuccess) return PKV_ERR_CUDA;
+    return PKV_OK;
 }
 
 }  // namespace pkv

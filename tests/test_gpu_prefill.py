@@ -75,3 +75,45 @@ def test_prefill_deterministic_and_matches_decode_of_last_token(pkv):
                          int(wl.kv_lens.max()), wl.softmax_scale)
     assert_attention_close(dec, ref[wl.cu_seqlens_q[1:] - 1], "decode of the last token")
     expect_no_device_error(pkv)
+
+
+def test_prefill_many_units_per_cta(pkv):
+    """~2400 work units over the persistent grid: exercises the cross-unit pipeline."""
+    rng = np.random.default_rng(25)
+    kl = rng.integers(1, 400, size=200)
+    ql = np.maximum(1, (kl * rng.uniform(0.2, 1.0, size=200)).astype(int))
+    ql = np.minimum(ql, kl)
+    wl, b, out, ref = _prefill_only(pkv, ql, kl, seed=25)
+    assert_attention_close(out, ref, "200 sequences, mid-block offsets")
+    expect_no_device_error(pkv)
+
+
+def test_prefill_long_sequence_with_prefix(pkv):
+    """Long rescale chains: 3000 new tokens after a 5192-token cached prefix."""
+    wl, b, out, ref = _prefill_only(pkv, [3000, 129], [8192, 129], seed=26)
+    assert_attention_close(out, ref, "3000 new tokens after a 5192-token prefix")
+    expect_no_device_error(pkv)
+
+
+def test_prefill_zero_length_queries(pkv):
+    wl, b, out, ref = _prefill_only(pkv, [0, 5, 0, 70], [10, 5, 300, 300], seed=27)
+    assert_attention_close(out, ref, "sequences with no new tokens")
+    expect_no_device_error(pkv)
+
+
+def test_prefill_large_score_range_forces_rescale(pkv):
+    """Scores growing along the keys make the row max climb by more than 2^8 several times."""
+    wl = W.build_workload("ramp", [200], [1000], seed=28)
+    vals = W.paged_values(wl)
+    ramp = torch.linspace(0.0, 6.0, wl.block_size * vals.k_cache.shape[0]).view(vals.k_cache.shape[0], wl.block_size, 1, 1)
+    vals.k_cache = (vals.k_cache.float() * ramp).to(torch.bfloat16)
+    vals.q = (vals.q.float() * 3.0).to(torch.bfloat16)
+    # a peaked softmax returns nearly single V rows; keep |o| moderate so bf16 output
+    # rounding stays inside the stated absolute tolerance
+    vals.v_cache = (vals.v_cache.float() * 0.25).to(torch.bfloat16)
+    b = GpuBatch(wl, vals)
+    out = b.run_prefill(pkv)
+    ref = pa.prefill_varlen(f32(vals.q), f32(vals.k_cache), f32(vals.v_cache), wl.cu_seqlens_q, wl.cu_seqlens_k,
+                            wl.block_tables, wl.block_size, wl.softmax_scale)
+    assert_attention_close(out, ref, "large score range")
+    expect_no_device_error(pkv)
