@@ -68,7 +68,9 @@ constexpr int SM_QA = 0;
 constexpr int SM_QB = SM_QA + TILE_BYTES;
 constexpr int SM_K = SM_QB + TILE_BYTES;          // 2 stages
 constexpr int SM_V = SM_K + 2 * TILE_BYTES;       // 2 stages
-constexpr int SM_BAR = SM_V + 2 * TILE_BYTES;
+constexpr int SM_STAGE = SM_V + 2 * TILE_BYTES;   // epilogue staging: 4 KiB per softmax warp
+constexpr int STAGE_WARP_BYTES = 32 * 128;
+constexpr int SM_BAR = SM_STAGE + 8 * STAGE_WARP_BYTES;
 enum {
     BAR_QF = 0, BAR_QE, BAR_KF, BAR_KF1, BAR_KE, BAR_KE1, BAR_VF, BAR_VF1, BAR_VE, BAR_VE1,
     BAR_SF, BAR_SF1, BAR_PF, BAR_PF1, BAR_OF, BAR_OF1, BAR_OE, BAR_OE1, BAR_DRAIN, NUM_BARS
@@ -80,7 +82,7 @@ struct Params {
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* block_tables;
-    const uint32_t* plan;     // [0] = number of (seq, pair) entries, then entries (seq << 16 | pair)
+    const uint4* plan;        // [0].x = number of (seq, pair) records; then {seq << 16 | pair, q_start, q_len, k_len}
     uint16_t* out;
     int max_blocks;
     int num_heads;
@@ -97,12 +99,14 @@ struct Ctl {
 };
 
 // Inlined on purpose: a call inside a setmaxnreg region cannot be register-allocated.
+// A waiting thread sleeps in try_wait (up to ~0.5 ms per try) instead of
+// spinning, so the warps it shares a scheduler with -- the MMA-issuing and
+// TMA warps -- keep their issue slots.
 __device__ __forceinline__ bool wait_phase(const Ctl& c, uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 500000u)) return true;
         if (*c.abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *c.abort = 1u;
@@ -114,7 +118,7 @@ __device__ __forceinline__ bool wait_phase(const Ctl& c, uint32_t bar, uint32_t 
 
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait_sleep(bar, parity, 500000u))
         if (global_ns() - t0 > kWaitLimitNs) return false;
     return true;
 }
@@ -135,16 +139,20 @@ struct Unit {
     int n[2];          // KV tiles of tile A and tile B (B may be 0)
 };
 
-__device__ __forceinline__ Unit unit_at(const Params& p, int idx) {
+// One 16-byte record per (seq, pair), so a unit's metadata is a single load that
+// can be issued a whole unit ahead of its use.
+__device__ __forceinline__ uint4 unit_record(const Params& p, int idx) {
+    return idx >= 0 ? __ldg(p.plan + 1 + idx / p.num_kv_heads) : make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ Unit unit_from(const Params& p, int idx, uint4 rec) {
     Unit u;
-    const uint32_t e = __ldg(p.plan + 1 + idx / p.num_kv_heads);
     u.g = idx % p.num_kv_heads;
-    u.seq = static_cast<int>(e >> 16);
-    u.pair = static_cast<int>(e & 0xffffu);
-    u.q_start = __ldg(p.cu_q + u.seq);
-    u.ql = __ldg(p.cu_q + u.seq + 1) - u.q_start;
-    const int k0 = __ldg(p.cu_k + u.seq);
-    u.kl = __ldg(p.cu_k + u.seq + 1) - k0;
+    u.seq = static_cast<int>(rec.x >> 16);
+    u.pair = static_cast<int>(rec.x & 0xffffu);
+    u.q_start = static_cast<int>(rec.y);
+    u.ql = static_cast<int>(rec.z);
+    u.kl = static_cast<int>(rec.w);
     u.offset = u.kl - u.ql;
     u.n[0] = kv_tiles(u.pair * UNIT_TOK, u.ql, u.offset);
     u.n[1] = kv_tiles(u.pair * UNIT_TOK + QTOK, u.ql, u.offset);
@@ -165,7 +173,7 @@ __device__ __forceinline__ int unit_index(int r, int total) {
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q,
                                                            const int32_t* __restrict__ cu_k, int num_seqs,
                                                            int max_blocks, int block_size, int max_cost,
-                                                           uint32_t* __restrict__ plan, int* err) {
+                                                           uint4* __restrict__ plan, int* err) {
     extern __shared__ int hist[];          // [max_cost + 1]
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int i = threadIdx.x; i <= max_cost; i += blockDim.x) hist[i] = 0;
@@ -191,7 +199,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
     if (threadIdx.x == 0) {
         int run = 0;
         for (int c = max_cost; c >= 0; --c) { const int x = hist[c]; hist[c] = run; run += x; }
-        plan[0] = static_cast<uint32_t>(run);
+        plan[0] = make_uint4(static_cast<uint32_t>(run), 0u, 0u, 0u);
     }
     __syncthreads();
     for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
@@ -201,7 +209,9 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
         for (int pr = 0; pr * UNIT_TOK < ql; ++pr) {
             const int cost = min(max_cost, kv_tiles(pr * UNIT_TOK, ql, off) + kv_tiles(pr * UNIT_TOK + QTOK, ql, off));
             const int pos = atomicAdd(&hist[cost], 1);
-            plan[1 + pos] = (static_cast<uint32_t>(s) << 16) | static_cast<uint32_t>(pr);
+            plan[1 + pos] = make_uint4((static_cast<uint32_t>(s) << 16) | static_cast<uint32_t>(pr),
+                                       static_cast<uint32_t>(cu_q[s]), static_cast<uint32_t>(ql),
+                                       static_cast<uint32_t>(kl));
         }
     }
 }
@@ -250,7 +260,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = misc[0];
     // everything above overlaps the plan kernel; global reads start here
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int total_units = static_cast<int>(__ldg(p.plan)) * p.num_kv_heads;
+    const int total_units = static_cast<int>(__ldg(p.plan).x) * p.num_kv_heads;
 
     // Each warpgroup runs its own branch to the kernel's end (no common tail, so
     // every instruction has one register budget); every branch ends at the same
@@ -261,10 +271,12 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) {
             int t = 0;           // KV tiles issued by this CTA
             int issued_k = 0, issued_v = 0, uq = 0;
-            for (int r = 0;; ++r) {
-                const int idx = unit_index(r, total_units);
-                if (idx < 0) break;
-                const Unit u = unit_at(p, idx);
+            int idx = unit_index(0, total_units);
+            uint4 rec = unit_record(p, idx);
+            for (int r = 0; idx >= 0; ++r) {
+                const Unit u = unit_from(p, idx, rec);
+                idx = unit_index(r + 1, total_units);
+                rec = unit_record(p, idx);            // in flight while this unit is issued
                 const int n = max(u.n[0], u.n[1]);
                 if (uq >= 1 && !wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1)) break;
                 const int qrow = u.q_start + u.pair * UNIT_TOK;
@@ -318,21 +330,28 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             int cntP[2] = {0, 0}, uact[2] = {0, 0};
             bool ok = true;
             int s_left = 0;      // S MMAs of the current unit not yet issued
+            // descriptors of every operand base; a K step only advances the start-address field
+            // (address >> 4 in the low 14 bits; shared addresses stay below 256 KiB, so no carry)
+            const uint64_t dq0 = kmajor_desc(sQ[0]), dq1 = kmajor_desc(sQ[1]);
+            const uint64_t dk0 = kmajor_desc(sK), dk1 = kmajor_desc(sK + TILE_BYTES);
+            const uint64_t dv0 = vmajor_desc(sV), dv1 = vmajor_desc(sV + TILE_BYTES);
             auto issue_s = [&](int X, int st) {
-                const uint32_t kbase = sK + st * TILE_BYTES;
+                const uint64_t da = X ? dq1 : dq0;
+                const uint64_t db = st ? dk1 : dk0;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t koff = (ks >> 2) * HALF_BYTES + (ks & 3) * 32;
-                    mma_ss(tmem + S_COL(X), kmajor_desc(sQ[X] + koff), kmajor_desc(kbase + koff), idesc_qk,
-                           ks > 0 ? 1u : 0u);
+                    const uint32_t koff = ((ks >> 2) * HALF_BYTES + (ks & 3) * 32) >> 4;
+                    mma_ss(tmem + S_COL(X), da + koff, db + koff, idesc_qk, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(BAR_SF + X));
                 if (--s_left == 0) mma_commit(bar(BAR_QE));   // the unit's Q tiles are no longer read
             };
-            for (int r = 0; ok; ++r) {
-                const int idx = unit_index(r, total_units);
-                if (idx < 0) break;
-                const Unit u = unit_at(p, idx);
+            int idx = unit_index(0, total_units);
+            uint4 rec = unit_record(p, idx);
+            for (int r = 0; ok && idx >= 0; ++r) {
+                const Unit u = unit_from(p, idx, rec);
+                idx = unit_index(r + 1, total_units);
+                rec = unit_record(p, idx);
                 const int n = max(u.n[0], u.n[1]);
                 s_left = u.n[0] + u.n[1];
                 if (!(ok = wait_phase(ctl, bar(BAR_QF), uq & 1))) break;
@@ -377,9 +396,9 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                                 v_tail_done = true;
                             }
-                            const uint32_t vbase = sV + st * TILE_BYTES;
+                            const uint64_t dvs = st ? dv1 : dv0;
                             for (int ks = 0; ks < ksteps; ++ks)
-                                mma_ts(tmem + O_COL(X), tmem + S_COL(X) + ks * 8, vmajor_desc(vbase + ks * 16 * 128),
+                                mma_ts(tmem + O_COL(X), tmem + S_COL(X) + ks * 8, dvs + ks * (16 * 128 >> 4),
                                        idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                             if (j == u.n[X] - 1) {
                                 mma_commit(bar(BAR_OF + X));
@@ -415,21 +434,23 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int X = warp >> 2;                  // 0: warps 0-3, 1: warps 4-7
         const int row = tid & 127;                // TMEM lane
         const int ti = row >> 1;
-        const int hh = row & 1;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + S_COL(X);
         const uint32_t o_tmem = tmem + lane_off + O_COL(X);
         const float sc = p.scale_log2;
         int cntS = 0, uact = 0;
         bool ok = true;
-        for (int r = 0; ok; ++r) {
-            const int idx = unit_index(r, total_units);
-            if (idx < 0) break;
-            const Unit u = unit_at(p, idx);
+        int idx = unit_index(0, total_units);
+        uint4 rec = unit_record(p, idx);
+        for (int r = 0; ok && idx >= 0; ++r) {
+            const Unit u = unit_from(p, idx, rec);
+            idx = unit_index(r + 1, total_units);
             const int nx = X ? u.n[1] : u.n[0];
-            if (nx == 0) continue;
+            if (nx == 0) {
+                rec = unit_record(p, idx);
+                continue;
+            }
             const int qi = u.pair * UNIT_TOK + X * QTOK + ti;
-            const bool row_valid = qi < u.ql;
             const int jmax = min(qi + u.offset, u.kl - 1);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < nx; ++j) {
@@ -511,25 +532,46 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!ok) break;
             ++uact;
             tc_fence_after();
+            rec = unit_record(p, idx);   // the next unit's record loads while this epilogue runs
+            // O / l -> bf16, 64 columns at a time: each thread writes its row into this warp's
+            // staging area (16-byte chunks XOR-swizzled by row, no bank conflicts), then the warp
+            // stores four 128-byte row halves per instruction
             const float inv = 1.f / l;
-            uint16_t* dst = p.out + (static_cast<int64_t>(u.q_start + qi) * p.num_heads + G * u.g + hh) * D;
+            uint8_t* stg = gbase + SM_STAGE + warp * STAGE_WARP_BYTES;
+            const uint32_t stg_s = smem_u32(stg);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t o[32];
-                tmem_ld32(o_tmem + 32 * c, o);
-                tmem_ld_wait();
-                if (row_valid) {
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+            for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(o_tmem + 64 * half + 32 * c, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int k = 4 * c + q;                  // 16-byte chunk of the 128-byte half row
                         uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-                        d4[v] = w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                        *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) * 16)) = w;
                     }
                 }
+                __syncwarp();
+#pragma unroll
+                for (int it = 0; it < 8; ++it) {
+                    const int rr = it * 4 + (lane >> 3);          // row of this warp's 32
+                    const int k = lane & 7;
+                    const uint4 w = ld_shared_v4(stg_s + rr * 128 + ((k ^ (rr & 7)) * 16));
+                    const int lrow = (warp & 3) * 32 + rr;        // TMEM lane = tile row
+                    const int tok = u.pair * UNIT_TOK + X * QTOK + (lrow >> 1);
+                    if (tok < u.ql) {
+                        uint16_t* d = p.out + (static_cast<int64_t>(u.q_start + tok) * p.num_heads + G * u.g +
+                                               (lrow & 1)) * D + 64 * half + 8 * k;
+                        *reinterpret_cast<uint4*>(d) = w;
+                    }
+                }
+                __syncwarp();
             }
             tc_fence_before();
             mbar_arrive(bar(BAR_OE + X));
@@ -548,7 +590,7 @@ constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(25
 
 size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q) {
     const size_t pairs = static_cast<size_t>(num_seqs) * ((max_seqlen_q + UNIT_TOK - 1) / UNIT_TOK);
-    return align256((pairs + 1) * 4);
+    return align256((pairs + 1) * 16);
 }
 
 pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
@@ -586,7 +628,7 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
     p.block_tables = a.block_tables;
-    p.plan = static_cast<const uint32_t*>(a.workspace);
+    p.plan = static_cast<const uint4*>(a.workspace);
     p.out = a.out;
     p.max_blocks = a.max_blocks;
     p.num_heads = a.num_heads;
@@ -612,7 +654,7 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
         configured_device = dev;
     }
     prefill_plan_kernel<<<1, 1024, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.max_blocks, a.block_size,
-                                                        max_cost, static_cast<uint32_t*>(a.workspace), err);
+                                                        max_cost, static_cast<uint4*>(a.workspace), err);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
 
     const int64_t max_units = static_cast<int64_t>(a.num_seqs) *
