@@ -137,6 +137,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def max_over_ranks(value, dist, device="cuda"):
+    """The slowest rank's time: every rank's timed region ends at the barrier after it."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(bytes_per_rank, ms_slowest, world_size):
+    """Whole-job throughput in GB/s: every rank processed its own replica of the workload."""
+    return bytes_per_rank * world_size / (ms_slowest * 1e-3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -308,12 +323,9 @@ def bench_headline(args, pkv, torch, dist, ws, rank, peaks):
     clock_rows = clocks.stop()
     elapsed_ms = start.elapsed_time(end)
     call_ms = [a.elapsed_time(b) for a, b in evs]
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist)
     ms_per_step = elapsed_ms / K
-    value = wl.kv_bytes_read * ws / (ms_per_step * 1e-3) / 1e9
+    value = weak_scaling_value(wl.kv_bytes_read, ms_per_step, ws)
     hbm, _, _, peak_kind = peaks
     call_mean = float(np.mean(call_ms))
     achieved = wl.kv_bytes_read / (call_mean * 1e-3) / 1e9
@@ -365,11 +377,8 @@ def bench_e2e(args, pkv, torch, step, dist, ws):
     e.record()
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / K
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": wl.kv_bytes_read * ws / (ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+    ms = max_over_ranks(ms, dist)
+    return {"value": weak_scaling_value(wl.kv_bytes_read, ms, ws), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K}
 
 
