@@ -5,9 +5,10 @@ Headline (one JSON line on stdout): a decode step of the decode-attention
 workload -- batch 64, Qwen3-0.6B attention shapes (16 query heads, 8 KV heads,
 head_dim 128, bf16), 256-token blocks, context lengths uniform in
 [512, 4096], physical blocks a random permutation of a pool 1.25x the blocks
-used.  One step = slot mapping + KV scatter of the new token + decode
-attention (split-K + combine), all through the C ABI.  value = KV bytes the
-attention reads per step / step time, in GB/s.
+used.  One step = the new token's slot, its KV write and the decode attention,
+through the C ABI call that fuses them (pkv_decode_append: split-K decode +
+combine launches); the same step through the three separate calls is reported
+beside it.  value = KV bytes the attention reads per step / step time, in GB/s.
 
 The same line carries:
   roofline      the decode attention call's achieved HBM GB/s (KV bytes per
@@ -278,20 +279,35 @@ class DecodeStep:
         self.ev = None
 
     def layer(self, i, q=None, k_new=None, v_new=None, events=None):
+        """One decode step of one layer: the new token's slot, its K/V write and the
+        attention, fused in pkv_decode_append (split-K decode + combine launches)."""
         v = self.layers[i]
         pkv, wl = self.pkv, self.wl
-        pkv.pkv_slot_mapping(self.block_tables, wl.num_blocks, wl.block_size, self.slots, context_lens=self.ctx)
-        pkv.pkv_store_kvcache(k_new if k_new is not None else v.k_new, v_new if v_new is not None else v.v_new,
-                              self.slots, v.k_cache, v.v_cache)
         if events is not None:
             events[0].record()
-        pkv.pkv_decode(q if q is not None else v.q, v.k_cache, v.v_cache, self.block_tables, self.ctx, self.max_ctx,
-                       wl.softmax_scale, out=self.out, workspace=self.ws)
+        pkv.pkv_decode_append(q if q is not None else v.q, k_new if k_new is not None else v.k_new,
+                              v_new if v_new is not None else v.v_new, v.k_cache, v.v_cache, self.block_tables,
+                              self.ctx, self.max_ctx, wl.softmax_scale, out=self.out, slot_mapping=self.slots,
+                              workspace=self.ws)
         if events is not None:
             events[1].record()
         return self.out
 
-    LAUNCHES_PER_LAYER = 4   # slot mapping, scatter, split-K decode, combine
+    def layer_unfused(self, i, events=None):
+        """The same step through the separate calls: slot mapping, scatter, decode."""
+        v = self.layers[i]
+        pkv, wl = self.pkv, self.wl
+        pkv.pkv_slot_mapping(self.block_tables, wl.num_blocks, wl.block_size, self.slots, context_lens=self.ctx)
+        pkv.pkv_store_kvcache(v.k_new, v.v_new, self.slots, v.k_cache, v.v_cache)
+        if events is not None:
+            events[0].record()
+        pkv.pkv_decode(v.q, v.k_cache, v.v_cache, self.block_tables, self.ctx, self.max_ctx, wl.softmax_scale,
+                       out=self.out, workspace=self.ws)
+        if events is not None:
+            events[1].record()
+        return self.out
+
+    LAUNCHES_PER_LAYER = 2   # fused split-K decode (slot + KV write + attention), combine
 
 
 def bench_headline(args, pkv, torch, dist, ws, rank, peaks):
@@ -332,12 +348,27 @@ def bench_headline(args, pkv, torch, dist, ws, rank, peaks):
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": profiled_traffic("decode_splitk_b64_traffic.json", DECODE_SRC),
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                "kernel": "pkv_decode call (split-K decode + combine), CUDA events on the launching stream",
+                "kernel": "pkv_decode_append call (split-K decode with the fused KV write + combine), "
+                          "CUDA events on the launching stream",
                 "algorithmic_bytes_per_launch": wl.kv_bytes_read}
+    # the same step through the three separate calls (4 launches), for comparison
+    K2 = max(10, K // 4)
+    su, eu = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        step.layer_unfused(0)
+    torch.cuda.synchronize()
+    su.record()
+    for _ in range(K2):
+        step.layer_unfused(0)
+    eu.record()
+    torch.cuda.synchronize()
+    unfused_ms = su.elapsed_time(eu) / K2
     e2e = bench_e2e(args, pkv, torch, step, dist, ws)
     res = dict(value=value, ms_per_step=ms_per_step, roofline=roofline, e2e=e2e,
                clocks=ClockSampler.summary(clock_rows), gpu_launches=K * DecodeStep.LAUNCHES_PER_LAYER,
-               config=decode_config_dict(wl), call_ms=call_mean)
+               config=decode_config_dict(wl), call_ms=call_mean,
+               unfused=dict(ms_per_step=unfused_ms, gbs=wl.kv_bytes_read / (unfused_ms * 1e-3) / 1e9,
+                            launches_per_step=4, calls="pkv_slot_mapping + pkv_store_kvcache + pkv_decode"))
     return res, cpu_arrays, wl
 
 
@@ -529,7 +560,7 @@ def main(argv=None):
     peaks = load_peaks()
 
     head, cpu_arrays, wl = bench_headline(args, pkv, torch, dist, ws, rank, peaks)
-    secondary = {}
+    secondary = {"unfused_decode_step": head["unfused"]}
     parts = set() if args.no_secondary else {x.strip() for x in args.parts.split(",") if x.strip()}
     if rank == 0:
         if "prefill" in parts:

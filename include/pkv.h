@@ -196,6 +196,34 @@ PKV_API pkv_status pkv_decode(const pkv_bf16 *q, const pkv_bf16 *k_cache, const 
                       pkv_stream_t stream);
 
 /*
+ * a1 + a2 + a4 in one call: the decode step with the KV write fused in.
+ * Visual atlas fig. 21 (the newest token's KV is written, then attention runs
+ * over the whole history) and the offline explainer's scope box (input tokens
+ * write KV first); slot rule of the atlas slot figure.
+ *
+ * For each sequence b with L = context_lens[b] > 0: the row of position L - 1
+ * (slot = block_tables[b][(L-1) / bs] * bs + (L-1) % bs) of every KV head
+ * receives k_new[b] / v_new[b], then out[b] is pkv_decode's result over the L
+ * keys, now including that row.  Same result as pkv_slot_mapping (context_lens
+ * form) + pkv_store_kvcache + pkv_decode, in two launches instead of four: the
+ * warp that loads a sequence's last KV chunk writes the new row first.
+ *
+ *   k_new, v_new  bf16 [batch, num_kv_heads, head_dim], contiguous
+ *   k_cache, v_cache  written at the new rows and read
+ *   slot_mapping  int32 [batch] output, or NULL: each new token's slot (-1 for
+ *                 a sequence with context_lens[b] == 0, which writes nothing)
+ *   workspace     as for pkv_decode
+ * A block id outside the pool skips the write and records PKV_DEVERR_BLOCK_ID.
+ */
+PKV_API pkv_status pkv_decode_append(const pkv_bf16 *q, const pkv_bf16 *k_new, const pkv_bf16 *v_new,
+                             pkv_bf16 *k_cache, pkv_bf16 *v_cache, const int32_t *block_tables,
+                             int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t batch,
+                             int32_t max_context_len, int32_t num_heads, int32_t num_kv_heads,
+                             int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                             float softmax_scale, pkv_bf16 *out, int32_t *slot_mapping,
+                             void *workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
  * Decode without any allocation.  The paper has no counterpart: this is a
  * library convenience for callers that cannot call cudaMalloc -- for example
  * a plugin inside a host runtime that owns all device memory and hands it only

@@ -30,7 +30,7 @@ __all__ = [
     "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
     "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
     "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error",
-    "decode_workspace", "pkv_decode_noalloc", "DEVERR",
+    "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "DEVERR",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +81,9 @@ def load() -> ctypes.CDLL:
         "pkv_decode": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
                                       _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_float, _c_ptr,
                                       _c_ptr, _c_size, _c_ptr]),
+        "pkv_decode_append": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr,
+                                             _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
+                                             _c_int32, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]),
         "pkv_decode_noalloc": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32,
                                               _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
                                               _c_float, _c_ptr, _c_ptr]),
@@ -253,6 +256,41 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
                              _ptr(context_lens), batch, int(max_context_len), hq, hkv, d, bs, nb,
                              float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
            "pkv_decode")
+    return out
+
+
+def pkv_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                      max_context_len: int, softmax_scale: float, out: Optional[torch.Tensor] = None,
+                      slot_mapping: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """Decode step with the KV write fused in: the new token's K/V go to position
+    context_lens[b] - 1, then decode attention over context_lens[b] keys."""
+    nb, bs, hkv, d = _pool_shape(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k_new, "k_new", torch.bfloat16, 3)
+    _check(v_new, "v_new", torch.bfloat16, 3)
+    _check(block_tables, "block_tables", torch.int32, 2)
+    _check(context_lens, "context_lens", torch.int32, 1)
+    batch, hq, dq = q.shape
+    if dq != d or context_lens.shape[0] != batch or block_tables.shape[0] != batch:
+        raise ValueError("q, context_lens and block_tables disagree")
+    if tuple(k_new.shape) != (batch, hkv, d) or tuple(v_new.shape) != (batch, hkv, d):
+        raise ValueError(f"k_new / v_new must be [{batch}, {hkv}, {d}]")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, 3)
+    if slot_mapping is not None:
+        _check(slot_mapping, "slot_mapping", torch.int32, 1)
+    if workspace is None:
+        workspace = decode_workspace(batch, hq, hkv, d, q.device)
+    _check(workspace, "workspace", torch.uint8, 1)
+    _raise(load().pkv_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), batch,
+                                    int(max_context_len), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
+                                    _ptr(slot_mapping), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "pkv_decode_append")
     return out
 
 

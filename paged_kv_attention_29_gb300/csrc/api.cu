@@ -251,6 +251,49 @@ pkv_status pkv_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16
     return launch_decode(a, err, as_stream(stream));
 }
 
+pkv_status pkv_decode_append(const pkv_bf16* q, const pkv_bf16* k_new, const pkv_bf16* v_new,
+                             pkv_bf16* k_cache, pkv_bf16* v_cache, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                             int32_t max_context_len, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, float softmax_scale, pkv_bf16* out,
+                             int32_t* slot_mapping, void* workspace, size_t workspace_bytes,
+                             pkv_stream_t stream) {
+    if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
+        !(softmax_scale == softmax_scale))
+        return PKV_ERR_INVALID_ARG;
+    if (!supported_shape(num_heads, num_kv_heads, head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+         reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) &
+        15)
+        return PKV_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+    int* err = device_error_word();
+    if (!err) return PKV_ERR_CUDA;
+    DecodeArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = out;
+    a.max_blocks = max_blocks_per_seq;
+    a.batch = batch;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.softmax_scale = softmax_scale;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slot_out = slot_mapping;
+    return launch_decode(a, err, as_stream(stream));
+}
+
 pkv_status pkv_sample(const float* logits, int32_t batch, int32_t vocab, int64_t row_stride,
                       const float* temperatures, uint64_t seed, uint64_t offset, int64_t* out_ids,
                       pkv_stream_t stream) {

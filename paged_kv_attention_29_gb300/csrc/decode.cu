@@ -59,6 +59,13 @@ struct Params {
     float* part_ml;        // [pieces][G][2]  (m, l)
     float* part_o;         // [pieces][G][D]
     int* err;
+    // fused KV write (pkv_decode_append): the new token of sequence b is written at
+    // position context_lens[b] - 1 before the chunk holding it is loaded
+    const uint16_t* k_new; // [batch, Hkv, D] or nullptr (no write)
+    const uint16_t* v_new;
+    uint16_t* k_pool;      // the pools the tensor maps read
+    uint16_t* v_pool;
+    int32_t* slot_out;     // [batch] or nullptr
 };
 
 __device__ __forceinline__ int seq_chunks(const int32_t* prefix, int b) { return prefix[b + 1] - prefix[b]; }
@@ -171,6 +178,9 @@ __device__ __forceinline__ void flush_piece(const Params& p, int slot, int lane,
     }
 }
 
+// kFused: also write this step's K/V row (pkv_decode_append); a separate instantiation so
+// that the plain decode compiles to the same code it had without the write.
+template <bool kFused>
 __global__ void __launch_bounds__(THREADS, 1)
 decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const Params p) {
@@ -179,6 +189,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageRegion);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + kStageRegion + WARPS * STAGES * 8);
     int32_t* tsum = prefix + (p.batch + 1);
+    int32_t* stage_phys = tsum + THREADS;      // [WARPS][STAGES]: physical block of each staged chunk
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -258,6 +269,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         if (lane == 0) {
             if (phys < 0 || phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, pc.b);
             const int s = issued % STAGES;
+            if (kFused) stage_phys[warp * STAGES + s] = phys;
             const uint32_t bar = bar_base + 8 * s;
             const uint32_t dst = stage_base + s * STAGE_BYTES;
             mbar_arrive_expect_tx(bar, STAGE_BYTES);
@@ -285,6 +297,15 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         for (int e = 0; e < 16; ++e) o[h][e] = 0.f;
     }
     int Lb = min(max(__ldg(p.context_lens + cc.b), 0), cap);
+    // fused KV write: this lane's 16 bytes of the segment's new row (lanes 0-15: K, 16-31: V)
+    // and the physical block of position L - 1, loaded at segment entry, used at its last chunk
+    uint4 kv_row = make_uint4(0, 0, 0, 0);
+    auto load_new_row = [&]() {
+        if (!kFused) return;
+        const int64_t src = static_cast<int64_t>(cc.b) * hkv + cc.g;
+        kv_row = __ldg(reinterpret_cast<const uint4*>((lane < 16 ? p.k_new : p.v_new) + src * D + (lane & 15) * 8));
+    };
+    load_new_row();
     bool failed = false;
     int consumed = 0;
 
@@ -295,6 +316,24 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const uint32_t kb = stage_base + s * STAGE_BYTES;
         const uint32_t vb = kb + KV_TILE_BYTES;
         const int n_valid = min(CHUNK, Lb - cc.c * CHUNK);
+        if (kFused && cc.c == cc.n - 1) {
+            // the chunk holding position L - 1: put this step's K/V row of head g into the staged
+            // tile (whatever the copy saw there) and into the pool, where later steps read it
+            const uint32_t r = (lane < 16 ? kb : vb) + (n_valid - 1) * (D * 2) + (lane & 15) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(r), "r"(kv_row.x), "r"(kv_row.y),
+                         "r"(kv_row.z), "r"(kv_row.w)
+                         : "memory");
+            const int off_in_block = (Lb - 1) % p.block_size;
+            const int kv_phys = stage_phys[warp * STAGES + s];   // the block the producer staged
+            const bool blk_ok = kv_phys >= 0 && kv_phys < p.num_blocks;
+            if (blk_ok) {
+                const int64_t row = (static_cast<int64_t>(kv_phys) * p.block_size + off_in_block) * hkv + cc.g;
+                *reinterpret_cast<uint4*>((lane < 16 ? p.k_pool : p.v_pool) + row * D + (lane & 15) * 8) = kv_row;
+            }
+            if (lane == 0 && cc.g == 0 && p.slot_out != nullptr)
+                p.slot_out[cc.b] = blk_ok ? kv_phys * p.block_size + off_in_block : -1;
+            __syncwarp();
+        }
 
         // scores: partial dot products of this lane's 16 dims, 8 tokens, 2 heads
         float part[8][G];
@@ -379,6 +418,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 cursor_next(cc, prefix, p.batch, hkv);
                 load_q(p, cc.b, cc.g, r, qf);
                 Lb = min(max(__ldg(p.context_lens + cc.b), 0), cap);
+                load_new_row();
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     m[h] = -INFINITY;
@@ -415,6 +455,7 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
     uint16_t* dst = out + static_cast<int64_t>(idx) * D + 4 * lane;
     if (n == 0) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        if (h == 0 && lane == 0 && p.slot_out != nullptr) p.slot_out[b] = -1;   // nothing was written
         return;
     }
     const int64_t W = p.total_warps;
@@ -453,7 +494,8 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
 }
 
 size_t dynamic_smem_bytes(int batch) {
-    return kStageRegion + WARPS * STAGES * 8 + static_cast<size_t>(batch + 1) * 4 + THREADS * 4 + 1024;
+    return kStageRegion + WARPS * STAGES * 8 + static_cast<size_t>(batch + 1) * 4 + THREADS * 4 + WARPS * STAGES * 4 +
+           1024;
 }
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -508,18 +550,29 @@ pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream) {
     ws += align256(pieces * G * 2 * 4);
     p.part_o = reinterpret_cast<float*>(ws);
     p.err = err;
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.k_pool = const_cast<uint16_t*>(a.k_cache);
+    p.v_pool = const_cast<uint16_t*>(a.v_cache);
+    p.slot_out = a.slot_out;
 
     const size_t smem = dynamic_smem_bytes(a.batch);
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        if (cudaFuncSetAttribute(decode_splitk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(dynamic_smem_bytes(MAX_BATCH))) != cudaSuccess)
+        const int max_smem = static_cast<int>(dynamic_smem_bytes(MAX_BATCH));
+        if (cudaFuncSetAttribute(decode_splitk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(decode_splitk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+                cudaSuccess)
             return PKV_ERR_CUDA;
         configured_device = dev;
     }
-    decode_splitk_kernel<<<W / WARPS, THREADS, smem, stream>>>(tm_k, tm_v, p);
+    if (p.k_new != nullptr)
+        decode_splitk_kernel<true><<<W / WARPS, THREADS, smem, stream>>>(tm_k, tm_v, p);
+    else
+        decode_splitk_kernel<false><<<W / WARPS, THREADS, smem, stream>>>(tm_k, tm_v, p);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     const int n_rows = a.batch * a.num_heads;
     decode_combine_kernel<<<(n_rows + 3) / 4, 128, 0, stream>>>(p, a.num_heads, a.out);

@@ -53,6 +53,9 @@ struct DecodeArgs {
     float softmax_scale;
     void* workspace;
     size_t workspace_bytes;
+    const uint16_t* k_new = nullptr;   // fused KV write (pkv_decode_append); nullptr: none
+    const uint16_t* v_new = nullptr;
+    int32_t* slot_out = nullptr;
 };
 
 int decode_total_warps();                                  // warps the decode grid runs

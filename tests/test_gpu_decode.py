@@ -112,3 +112,51 @@ def test_decode_flags_block_id_outside_pool(pkv):
     pkv.pkv_decode(b.q, b.k_cache, b.v_cache, bt, b.kv_lens, int(wl.kv_lens.max()), wl.softmax_scale)
     code, info = pkv.pkv_get_device_error(clear=True)
     assert code == 1 and info == 1
+
+
+@pytest.mark.parametrize("name", ["tiny-decode", "decode-b64", "long-decode"])
+def test_decode_append_matches_oracle(pkv, name):
+    """KV write fused into decode: pool bit-exact, slots bit-exact, output vs the fp64 oracle."""
+    wl = W.ALL[name]()
+    b = GpuBatch(wl, W.paged_values(wl, poison_unreferenced=True))
+    slots = torch.full((wl.batch,), -7, dtype=torch.int32, device="cuda")
+    out = pkv.pkv_decode_append(b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.block_tables, b.kv_lens,
+                                int(wl.kv_lens.max()), wl.softmax_scale, slot_mapping=slots)
+    kc, vc = b.oracle_pools()
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), b.oracle_slots())
+    assert np.array_equal(bits(b.k_cache), bits(torch.from_numpy(kc).to(torch.bfloat16)))
+    assert np.array_equal(bits(b.v_cache), bits(torch.from_numpy(vc).to(torch.bfloat16)))
+    assert_attention_close(out, b.oracle_decode(pools=(kc, vc)), name)
+    expect_no_device_error(pkv)
+
+
+def test_decode_append_bit_identical_to_unfused_path(pkv):
+    wl = W.decode_b64(batch=32)
+    vals = W.paged_values(wl)
+    fused = GpuBatch(wl, vals)
+    plain = GpuBatch(wl, vals)
+    o1 = pkv.pkv_decode_append(fused.q, fused.k_new, fused.v_new, fused.k_cache, fused.v_cache, fused.block_tables,
+                               fused.kv_lens, int(wl.kv_lens.max()), wl.softmax_scale)
+    plain.run_slots_and_store(pkv, decode=True)
+    o2 = plain.run_decode(pkv)
+    assert np.array_equal(bits(o1), bits(o2))
+    assert np.array_equal(bits(fused.k_cache), bits(plain.k_cache))
+    expect_no_device_error(pkv)
+
+
+def test_decode_append_zero_context_writes_nothing(pkv):
+    kv_lens = np.array([5, 0, 300, 0], dtype=np.int32)
+    wl = W.build_workload("zeros", np.ones(4, np.int32), kv_lens, seed=16)
+    vals = W.paged_values(wl)
+    b = GpuBatch(wl, vals)
+    before = bits(b.k_cache).copy()
+    slots = torch.full((4,), 99, dtype=torch.int32, device="cuda")
+    out = pkv.pkv_decode_append(b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.block_tables, b.kv_lens, 300,
+                                wl.softmax_scale, slot_mapping=slots)
+    s = slots.cpu().tolist()
+    assert s[1] == -1 and s[3] == -1 and s[0] >= 0 and s[2] >= 0
+    after = bits(b.k_cache)
+    changed = np.argwhere((before != after).reshape(wl.num_blocks, wl.block_size, -1).any(axis=2))
+    assert len(changed) == 2                                   # one row for each non-empty sequence
+    assert torch.count_nonzero(out[1]).item() == 0 and torch.count_nonzero(out[3]).item() == 0
+    expect_no_device_error(pkv)
