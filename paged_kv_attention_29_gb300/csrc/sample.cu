@@ -97,21 +97,54 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
         const int per = (nquads + CLUSTER - 1) / CLUSTER;
         const int q0 = rank * per;
         const int q1 = min(nquads, q0 + per);
-        for (int qd = q0 + tid; qd < q1; qd += THREADS) {
-            const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(qd), c1, c2, 0u), key0, key1);
-            const int col = qd * 4;
-            if (vec_ok && col + 3 < vocab) {
-                const float4 l4 = __ldcs(reinterpret_cast<const float4*>(lrow + col));
-                consider(l4.x, inv_t, x.x, col, bk, bi);
-                consider(l4.y, inv_t, x.y, col + 1, bk, bi);
-                consider(l4.z, inv_t, x.z, col + 2, bk, bi);
-                consider(l4.w, inv_t, x.w, col + 3, bk, bi);
-            } else {
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        // Pruning.  With t = best - l/T, an element can beat `best` only if
+        // -ln(-ln u) > t, i.e. -ln u < e^-t; since -ln u >= 1 - u that needs
+        // 1 - u < e^-t.  And -ln(-ln u) <= 16.64 for every u the generator makes
+        // (u <= 1 - 2^-24), so a quad whose largest l/T + 16.7 is below `best` has
+        // no candidate at all and skips its Philox call.  `best` is the warp's
+        // running maximum; t carries a 1e-3 margin so rounding and exact ties are
+        // always decided by the exact key.  Skipped elements cannot change the
+        // winner: some element of the warp already has a larger key.
+        const int iters = (q1 - q0 + THREADS - 1) / THREADS;     // uniform across the CTA
+        float wbest = -INFINITY;
+        for (int it = 0; it < iters; ++it) {
+            const int qd = q0 + it * THREADS + tid;
+            if (qd < q1) {
+                const int col = qd * 4;
+                float l[4];
+                if (vec_ok && col + 3 < vocab) {
+                    const float4 l4 = __ldcs(reinterpret_cast<const float4*>(lrow + col));
+                    l[0] = l4.x; l[1] = l4.y; l[2] = l4.z; l[3] = l4.w;
+                } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (col + e < vocab) consider(__ldcs(lrow + col + e), inv_t, xs[e], col + e, bk, bi);
+                    for (int e = 0; e < 4; ++e) l[e] = (col + e < vocab) ? __ldcs(lrow + col + e) : -INFINITY;
+                }
+                const float best = fmaxf(bk, wbest);
+                const float lmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+                // (NaN logits fail this test and go through the exact path, which rejects them)
+                if (!(lmax * inv_t + 16.7f < best)) {
+                    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(qd), c1, c2, 0u), key0, key1);
+                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (col + e >= vocab) continue;
+                        const float t = best - l[e] * inv_t - 1e-3f;
+                        if (t > 0.f) {
+                            // 1 - u exactly: (2^24 - (2 (x >> 9) + 1)) 2^-24
+                            const float one_minus_u =
+                                __uint2float_rn(16777216u - (2u * (xs[e] >> 9) + 1u)) * 5.9604644775390625e-08f;
+                            const float bound = exp2f(-t * 1.4426950408889634f) * 1.001f;
+                            if (one_minus_u >= bound) continue;
+                        }
+                        consider(l[e], inv_t, xs[e], col + e, bk, bi);
+                    }
+                }
             }
+            // share the running best across the warp
+            float m = bk;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            wbest = m;
         }
     } else if (rank == 0 && tid == 0) {
         record_error(err, PKV_DEVERR_TEMPERATURE, row);
