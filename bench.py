@@ -514,6 +514,7 @@ def bench_full_step(args, pkv, torch, peaks):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / K
     sample_ms = float(np.mean([a.elapsed_time(b) for a, b in samp]))
+    graph_ms = bench_full_step_graph(pkv, torch, st, s_in, K)
     kv = wl.kv_bytes_read * wl.num_layers
     logits_bytes = wl.batch * W.VOCAB_QWEN3 * 4
     res = {"workload": "full decode step: 28 layers x (slot map + scatter + decode), batch 256, context "
@@ -521,10 +522,46 @@ def bench_full_step(args, pkv, torch, peaks):
            "tok_per_s": wl.batch / (ms * 1e-3), "step_ms": ms, "kv_gbs": (kv + logits_bytes) / (ms * 1e-3) / 1e9,
            "sampler_ms": sample_ms, "sampler_gbs": logits_bytes / (sample_ms * 1e-3) / 1e9,
            "kv_bytes_per_step": kv, "steps": K,
-           "gpu_launches_per_step": wl.num_layers * DecodeStep.LAUNCHES_PER_LAYER + 1}
+           "gpu_launches_per_step": wl.num_layers * DecodeStep.LAUNCHES_PER_LAYER + 1,
+           "graph": {"step_ms": graph_ms, "tok_per_s": wl.batch / (graph_ms * 1e-3),
+                     "how": "the step (28 x pkv_decode_append + pkv_sample_dev + noise-offset update) "
+                            "captured once in a CUDA graph and replayed"}}
     del st
     torch.cuda.empty_cache()
     return res
+
+
+def bench_full_step_graph(pkv, torch, st, s_in, K):
+    """The full decode step captured in a CUDA graph, replayed K times."""
+    wl = st.wl
+    ids = torch.empty(wl.batch, dtype=torch.int64, device="cuda")
+    seed_offset = torch.tensor([s_in.seed, 0], dtype=torch.int64, device="cuda")
+
+    def step():
+        for layer in range(wl.num_layers):
+            st.layer(layer)
+        pkv.pkv_sample_dev(s_in.logits, s_in.temperatures, seed_offset, out_ids=ids)
+        seed_offset[1:].add_(wl.batch)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        g.replay()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(K):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / K
 
 
 def main(argv=None):

@@ -273,6 +273,18 @@ PKV_API pkv_status pkv_sample(const float *logits, int32_t batch, int32_t vocab,
                       int64_t *out_ids, pkv_stream_t stream);
 
 /*
+ * pkv_sample with the noise seed and row offset read from DEVICE memory:
+ * seed_offset = uint64 [2] = {seed, offset}, 8-byte aligned, read when the
+ * kernel runs.  A captured CUDA graph can then replay the sampler with fresh
+ * noise by updating that buffer between replays (atlas fig. 26: a replay
+ * reads new inputs from pre-allocated buffers).  Same result as pkv_sample
+ * with those values.
+ */
+PKV_API pkv_status pkv_sample_dev(const float *logits, int32_t batch, int32_t vocab, int64_t row_stride,
+                          const float *temperatures, const uint64_t *seed_offset, int64_t *out_ids,
+                          pkv_stream_t stream);
+
+/*
  * Read (and optionally clear) the current device's error word.  HOST output
  * pointers.  Synchronises the device.  code = PKV_DEVERR_*; info = a value
  * describing where (e.g. the sequence or token index).

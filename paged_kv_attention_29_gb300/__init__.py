@@ -30,7 +30,7 @@ __all__ = [
     "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
     "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
     "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error",
-    "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "DEVERR",
+    "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "pkv_sample_dev", "DEVERR",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -89,6 +89,7 @@ def load() -> ctypes.CDLL:
                                               _c_float, _c_ptr, _c_ptr]),
         "pkv_sample": (ctypes.c_int, [_c_ptr, _c_int32, _c_int32, _c_int64, _c_ptr, _c_u64, _c_u64, _c_ptr,
                                       _c_ptr]),
+        "pkv_sample_dev": (ctypes.c_int, [_c_ptr, _c_int32, _c_int32, _c_int64, _c_ptr, _c_ptr, _c_ptr, _c_ptr]),
         "pkv_get_device_error": (ctypes.c_int, [ctypes.POINTER(_c_int32), ctypes.POINTER(_c_int32), _c_int32]),
     }
     for name, (res, args) in sig.items():
@@ -330,6 +331,26 @@ def pkv_sample(logits: torch.Tensor, temperatures: torch.Tensor, seed: int, offs
     _raise(load().pkv_sample(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures),
                              int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(out_ids),
                              _stream(stream)), "pkv_sample")
+    return out_ids
+
+
+def pkv_sample_dev(logits: torch.Tensor, temperatures: torch.Tensor, seed_offset: torch.Tensor,
+                   out_ids: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pkv_sample with {seed, offset} read from a device int64 tensor of 2 elements
+    (so a captured CUDA graph can advance the noise between replays)."""
+    _check(logits, "logits", torch.float32, 2, contiguous=False)
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous")
+    _check(temperatures, "temperatures", torch.float32, 1)
+    _check(seed_offset, "seed_offset", torch.int64, 1)
+    if seed_offset.numel() != 2:
+        raise ValueError("seed_offset holds {seed, offset}")
+    batch, vocab = logits.shape
+    if out_ids is None:
+        out_ids = torch.empty(batch, dtype=torch.int64, device=logits.device)
+    _check(out_ids, "out_ids", torch.int64, 1)
+    _raise(load().pkv_sample_dev(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures), _ptr(seed_offset),
+                                 _ptr(out_ids), _stream(stream)), "pkv_sample_dev")
     return out_ids
 
 

@@ -303,7 +303,22 @@ pkv_status pkv_sample(const float* logits, int32_t batch, int32_t vocab, int64_t
     if (batch > 65535) return PKV_ERR_UNSUPPORTED;
     int* err = device_error_word();
     if (!err) return PKV_ERR_CUDA;
-    const cudaError_t e = launch_sample(logits, batch, vocab, row_stride, temperatures, seed, offset, out_ids,
+    const cudaError_t e = launch_sample(logits, batch, vocab, row_stride, temperatures, seed, offset, nullptr,
+                                        out_ids, err, as_stream(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_sample_dev(const float* logits, int32_t batch, int32_t vocab, int64_t row_stride,
+                          const float* temperatures, const uint64_t* seed_offset, int64_t* out_ids,
+                          pkv_stream_t stream) {
+    if (batch < 0 || vocab <= 0 || row_stride < vocab) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!logits || !temperatures || !out_ids || !seed_offset) return PKV_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(seed_offset) & 7) return PKV_ERR_INVALID_ARG;
+    if (batch > 65535) return PKV_ERR_UNSUPPORTED;
+    int* err = device_error_word();
+    if (!err) return PKV_ERR_CUDA;
+    const cudaError_t e = launch_sample(logits, batch, vocab, row_stride, temperatures, 0, 0, seed_offset, out_ids,
                                         err, as_stream(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

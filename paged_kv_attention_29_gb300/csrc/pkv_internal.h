@@ -91,6 +91,6 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream);
 // ---- a5 ---------------------------------------------------------------------
 cudaError_t launch_sample(const float* logits, int batch, int vocab, int64_t row_stride,
                           const float* temperatures, uint64_t seed, uint64_t offset,
-                          int64_t* out_ids, int* err, cudaStream_t stream);
+                          const uint64_t* seed_offset, int64_t* out_ids, int* err, cudaStream_t stream);
 
 }  // namespace pkv

@@ -72,7 +72,8 @@ __device__ __forceinline__ void consider(float logit, float inv_t, uint32_t x, i
 __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS)
 sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stride,
                    const float* __restrict__ temperatures, uint32_t key0, uint32_t key1,
-                   uint64_t offset, int vec_ok, int64_t* __restrict__ out_ids, int* err) {
+                   uint64_t offset, const uint64_t* __restrict__ seed_offset, int vec_ok,
+                   int64_t* __restrict__ out_ids, int* err) {
     __shared__ float s_key[THREADS / 32];
     __shared__ int s_idx[THREADS / 32];
     __shared__ float c_key;
@@ -83,6 +84,12 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
     const int row = blockIdx.y;
     const int tid = threadIdx.x;
     const float T = __ldg(temperatures + row);
+    if (seed_offset != nullptr) {          // seed and row offset from device memory
+        const uint64_t sd = __ldg(seed_offset);
+        key0 = static_cast<uint32_t>(sd);
+        key1 = static_cast<uint32_t>(sd >> 32);
+        offset = __ldg(seed_offset + 1);
+    }
     const bool t_ok = (T > 0.f) && (T < INFINITY);
 
     float bk = -INFINITY;
@@ -183,14 +190,14 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
 
 cudaError_t launch_sample(const float* logits, int batch, int vocab, int64_t row_stride,
                           const float* temperatures, uint64_t seed, uint64_t offset,
-                          int64_t* out_ids, int* err, cudaStream_t stream) {
+                          const uint64_t* seed_offset, int64_t* out_ids, int* err, cudaStream_t stream) {
     if (batch == 0) return cudaSuccess;
     const int vec_ok = ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) && (row_stride % 4 == 0);
     dim3 grid(CLUSTER, batch);
     sample_race_kernel<<<grid, THREADS, 0, stream>>>(logits, vocab, row_stride, temperatures,
                                                      static_cast<uint32_t>(seed),
-                                                     static_cast<uint32_t>(seed >> 32), offset, vec_ok,
-                                                     out_ids, err);
+                                                     static_cast<uint32_t>(seed >> 32), offset, seed_offset,
+                                                     vec_ok, out_ids, err);
     return cudaGetLastError();
 }
 

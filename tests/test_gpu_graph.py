@@ -1,0 +1,73 @@
+"""A decode step captured in a CUDA graph and replayed (atlas fig. 26: a replay
+reads new inputs from pre-allocated buffers; shapes and addresses are fixed,
+values may change).  The captured step -- two layers of pkv_decode_append and
+pkv_sample_dev, whose noise offset lives in device memory and advances inside
+the graph -- must give, replay after replay, exactly what the eager calls give."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from pkv_testutil import bits, expect_no_device_error
+
+pytestmark = pytest.mark.gpu
+
+
+def test_decode_step_graph_replay_matches_eager(pkv):
+    wl = W.decode_b64(batch=16, lo=100, hi=900)
+    layers = [W.paged_values(wl, device="cuda", layer=i) for i in range(2)]
+    eager_pools = [(v.k_cache.clone(), v.v_cache.clone()) for v in layers]
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    ctx = torch.from_numpy(wl.kv_lens).cuda()
+    ws = pkv.decode_workspace(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim)
+    s_in = W.sampler_inputs(batch=wl.batch, vocab=5000, device="cuda")
+    outs = [torch.empty_like(v.q) for v in layers]
+    ids = torch.empty(wl.batch, dtype=torch.int64, device="cuda")
+    seed_offset = torch.tensor([s_in.seed, 0], dtype=torch.int64, device="cuda")
+    max_ctx = int(wl.kv_lens.max())
+
+    def step(pools):
+        for i, v in enumerate(layers):
+            pkv.pkv_decode_append(v.q, v.k_new, v.v_new, pools[i][0], pools[i][1], bt, ctx, max_ctx,
+                                  wl.softmax_scale, out=outs[i], workspace=ws)
+        pkv.pkv_sample_dev(s_in.logits, s_in.temperatures, seed_offset, out_ids=ids)
+        seed_offset[1:].add_(wl.batch)              # next replay draws fresh noise
+
+    graph_pools = [(v.k_cache, v.v_cache) for v in layers]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(graph_pools)                            # first call on the device: set-up before capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(graph_pools)
+    seed_offset[1] = 0
+    for replay in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        got_out = [bits(o).copy() for o in outs]
+        got_ids = ids.cpu().clone()
+        # eager: the same calls with the offset this replay used
+        for i, v in enumerate(layers):
+            ref = pkv.pkv_decode_append(v.q, v.k_new, v.v_new, eager_pools[i][0], eager_pools[i][1], bt, ctx,
+                                        max_ctx, wl.softmax_scale, workspace=ws)
+            assert np.array_equal(bits(ref), got_out[i])
+        ref_ids = pkv.pkv_sample(s_in.logits, s_in.temperatures, s_in.seed, offset=replay * wl.batch)
+        assert torch.equal(ref_ids.cpu(), got_ids)
+    for i in range(2):
+        assert np.array_equal(bits(eager_pools[i][0]), bits(graph_pools[i][0]))
+    first = pkv.pkv_sample(s_in.logits, s_in.temperatures, s_in.seed, offset=0).cpu()
+    second = pkv.pkv_sample(s_in.logits, s_in.temperatures, s_in.seed, offset=wl.batch).cpu()
+    assert not torch.equal(first, second)            # the offset really changes the draw
+    expect_no_device_error(pkv)
+
+
+def test_sample_dev_equals_sample(pkv):
+    s_in = W.sampler_inputs(batch=32, vocab=20000, seed=41, device="cuda")
+    so = torch.tensor([12345, 77], dtype=torch.int64, device="cuda")
+    a = pkv.pkv_sample_dev(s_in.logits, s_in.temperatures, so)
+    b = pkv.pkv_sample(s_in.logits, s_in.temperatures, 12345, offset=77)
+    assert torch.equal(a, b)
+    expect_no_device_error(pkv)
