@@ -18,5 +18,7 @@ sampler
     Philox4x32-10 (the counter-based generator both sides implement from its
     published definition), the exponential noise drawn from it, and the
     temperature sampler's exponential race.
+rope
+    rotary position embedding of Q and K before the KV write (V untouched).
 """
-from . import paged_attention, sampler  # noqa: F401
+from . import paged_attention, rope, sampler  # noqa: F401

@@ -345,3 +345,64 @@ def test_race_frequencies_match_softmax():
     freq = np.bincount(ids, minlength=4) / n
     sigma = np.sqrt(p * (1 - p) / n)
     assert np.all(np.abs(freq - p) < 4 * sigma), (freq, p)
+
+
+# ---------------------------------------------------------------------------
+# Rotary position embedding (atlas fig. 19)
+# ---------------------------------------------------------------------------
+
+from oracle import rope as rp
+
+
+def test_rope_single_pair_is_the_2d_rotation():
+    """d = 2: one pair, frequency base^0 = 1, so the angle is the position itself."""
+    x = np.array([[[0.6, -1.3]]])
+    for pos in (0.0, 1.0, 2.5, 7.0):
+        out = rp.rope(x, [pos], base=1e6)[0, 0]
+        c, s = math.cos(pos), math.sin(pos)
+        np.testing.assert_allclose(out, [0.6 * c + 1.3 * s, -1.3 * c + 0.6 * s], rtol=0, atol=1e-15)
+    # quarter turn: (1, 0) -> (0, 1), counter-clockwise
+    np.testing.assert_allclose(rp.rope(np.array([[[1.0, 0.0]]]), [math.pi / 2], 1e6)[0, 0], [0.0, 1.0], atol=1e-15)
+
+
+def test_rope_identity_at_zero_and_norm_per_pair():
+    rng = np.random.default_rng(30)
+    x = rng.standard_normal((3, 2, 8))
+    np.testing.assert_array_equal(rp.rope(x, [0, 0, 0], 1e4), x)
+    y = rp.rope(x, [1, 17, 300], 1e4)
+    for i in range(4):
+        np.testing.assert_allclose(np.hypot(y[..., i], y[..., i + 4]), np.hypot(x[..., i], x[..., i + 4]),
+                                   rtol=1e-13)
+
+
+def test_rope_composes_and_inverts():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((1, 3, 16))
+    a = rp.rope(rp.rope(x, [5], 1e4), [11], 1e4)
+    np.testing.assert_allclose(a, rp.rope(x, [16], 1e4), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(rp.rope(rp.rope(x, [9], 1e4), [-9], 1e4), x, rtol=0, atol=1e-12)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    """<R(m) q, R(n) k> = <R(m-n) q, k>: what makes RoPE a position encoding for attention."""
+    rng = np.random.default_rng(32)
+    q = rng.standard_normal((1, 1, 32))
+    k = rng.standard_normal((1, 1, 32))
+    for m, n in [(10, 3), (100, 64), (7, 7)]:
+        lhs = float(np.sum(rp.rope(q, [m], 1e6) * rp.rope(k, [n], 1e6)))
+        rhs = float(np.sum(rp.rope(q, [m - n], 1e6) * k))
+        assert lhs == pytest.approx(rhs, abs=1e-10)
+
+
+def test_rope_store_rotates_q_and_k_not_v():
+    rng = np.random.default_rng(33)
+    q = rng.standard_normal((2, 4, 8))
+    k = rng.standard_normal((2, 2, 8))
+    v = rng.standard_normal((2, 2, 8))
+    kc = np.zeros((2, 4, 2, 8))
+    vc = np.zeros((2, 4, 2, 8))
+    qr, kc2, vc2 = rp.rope_store_kvcache(q, kc, vc, k, v, [3, 5], [1, 6], 4, 1e4)
+    np.testing.assert_array_equal(vc2[0, 1], v[0])
+    np.testing.assert_array_equal(vc2[1, 2], v[1])
+    np.testing.assert_allclose(kc2[1, 2], rp.rope(k, [3, 5], 1e4)[1], atol=1e-15)
+    np.testing.assert_allclose(qr, rp.rope(q, [3, 5], 1e4), atol=1e-15)
