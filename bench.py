@@ -413,8 +413,25 @@ def bench_e2e(args, pkv, torch, step, dist, ws):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": K}
 
 
-def flush_l2(torch, buf):
-    buf.add_(1)
+class L2Flush:
+    """Evict L2 between timed calls: write a buffer twice the size of L2, then read another one.
+
+    The read pass pushes the written lines' write-backs to DRAM before the timed
+    region starts, so the next call finds clean, unrelated lines in L2 and pays
+    neither for its own inputs being cached nor for the flush's dirty data."""
+
+    def __init__(self, torch, dev="cuda"):
+        n = 2 * L2_BYTES // 4
+        self.w = torch.empty(n, dtype=torch.float32, device=dev)
+        self.r = torch.zeros(n, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.add_(1)
+        self.r.amax()
+
+
+def flush_l2(torch, flush):
+    flush()
 
 
 def bench_prefill(args, pkv, torch, peaks):
@@ -426,7 +443,7 @@ def bench_prefill(args, pkv, torch, peaks):
     cu_k = torch.from_numpy(wl.cu_seqlens_k).to(dev)
     slots = torch.empty(wl.total_q, dtype=torch.int32, device=dev)
     out = torch.empty_like(v.q)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev)
     pairs = 0
     for ql, kl in zip(wl.q_lens.astype(np.int64), wl.kv_lens.astype(np.int64)):
         pairs += ql * (kl - ql) + ql * (ql + 1) // 2      # unmasked (query, key) pairs per head
@@ -463,8 +480,52 @@ def bench_prefill(args, pkv, torch, peaks):
                         "per group of 4, Hq 16, Hkv 8, d 128, bf16",
             "tflops": tflops, "unit": "TFLOP/s", "algorithmic_flops": int(flops), "call_ms_median": call,
             "step_ms_median": float(np.median(step_ms)), "frac_of_bf16_peak": tflops / bf16,
-            "peak": bf16, "peak_source": kind, "steps": K, "l2": "flushed between steps (256 MB write)",
+            "peak": bf16, "peak_source": kind, "steps": K, "l2": "flushed between steps (256 MB write, then 256 MB clean read)",
             "total_q": wl.total_q}
+
+
+def bench_rope_store(args, pkv, torch, peaks):
+    """RoPE fused into the KV write over the prefill workload's tokens, against the plain scatter."""
+    wl = W.prefill_prefix()
+    dev = "cuda"
+    v = W.paged_values(wl, device=dev)
+    n = wl.total_q
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    cu_q = torch.from_numpy(wl.cu_seqlens_q).to(dev)
+    cu_k = torch.from_numpy(wl.cu_seqlens_k).to(dev)
+    slots = torch.empty(n, dtype=torch.int32, device=dev)
+    pkv.pkv_slot_mapping(bt, wl.num_blocks, wl.block_size, slots, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
+    pos = torch.from_numpy(np.concatenate([np.arange(kl - ql, kl) for ql, kl in zip(wl.q_lens, wl.kv_lens)])
+                           .astype(np.int32)).to(dev)
+    q_out = torch.empty_like(v.q)
+    flush = L2Flush(torch, dev)
+    q_row, kv_row = wl.num_heads * wl.head_dim * 2, wl.num_kv_heads * wl.head_dim * 2
+    rope_bytes = n * (2 * q_row + 4 * kv_row + 8)        # q in/out, k in/out, v in/out, position, slot
+    store_bytes = n * (4 * kv_row + 4)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(max(10, min(100, args.steps // 30))):
+            flush_l2(torch, flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return float(np.median(ms))
+
+    rope_ms = timed(lambda: pkv.pkv_rope_store_kvcache(v.q, v.k_new, v.v_new, pos, slots, v.k_cache, v.v_cache,
+                                                       1e6, q_out=q_out))
+    store_ms = timed(lambda: pkv.pkv_store_kvcache(v.k_new, v.v_new, slots, v.k_cache, v.v_cache))
+    gbs = rope_bytes / (rope_ms * 1e-3) / 1e9
+    return {"workload": f"rotary embedding + KV write of the prefill workload's {n} tokens (Hq 16, Hkv 8, d 128, "
+                        "base 1e6)", "gbs": gbs, "unit": "GB/s", "call_ms_median": rope_ms,
+            "frac_of_hbm": gbs / peaks[0], "algorithmic_bytes": int(rope_bytes),
+            "plain_store_ms_median": store_ms, "plain_store_gbs": store_bytes / (store_ms * 1e-3) / 1e9,
+            "l2": "flushed between calls (256 MB write, then 256 MB clean read)"}
 
 
 def bench_long_decode(args, pkv, torch, peaks):
@@ -571,8 +632,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-secondary", action="store_true", help="headline only")
-    ap.add_argument("--parts", default="prefill,long,full",
-                    help="secondary workloads to run: any of prefill,long,full")
+    ap.add_argument("--parts", default="prefill,long,full,rope",
+                    help="secondary workloads to run: any of prefill,long,full,rope")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args(argv)
@@ -606,6 +667,8 @@ def main(argv=None):
             secondary["long_decode"] = bench_long_decode(args, pkv, torch, peaks)
         if "full" in parts:
             secondary["full_step"] = bench_full_step(args, pkv, torch, peaks)
+        if "rope" in parts:
+            secondary["rope_store"] = bench_rope_store(args, pkv, torch, peaks)
     code, info = pkv.pkv_get_device_error(clear=True)
     if code:
         raise RuntimeError(f"device error {code} ({pkv.DEVERR.get(code)}), info {info}")

@@ -9,6 +9,7 @@
  *   a3  pkv_prefill_varlen   varlen prefill attention, position-offset causal mask
  *   a4  pkv_decode           single-token decode attention over the block tables
  *   a5  pkv_sample           temperature sampling by exponential race
+ *   f2  pkv_rope_store_kvcache  rotary embedding of Q/K fused into the a2 write
  *
  * Conventions shared by every call
  * --------------------------------
@@ -125,6 +126,38 @@ PKV_API pkv_status pkv_store_kvcache(const pkv_bf16 *k, const pkv_bf16 *v, int64
                              const int32_t *slot_mapping, pkv_bf16 *k_cache, pkv_bf16 *v_cache,
                              int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                              int32_t head_dim, pkv_stream_t stream);
+
+/*
+ * f2. Rotary position embedding fused into the KV write.
+ * Visual atlas, fig. 19: each head of d elements forms d/2 two-dimensional
+ * pairs; pair i of a token at position p turns by p * rope_base^(-2i/d)
+ * radians, (a, b) -> (a cos - b sin, b cos + a sin).  Q and K are rotated,
+ * V is not.  Pair i couples elements i and i + d/2 of the head.
+ *
+ * For each token t < n_tokens: every head of q[t] (num_heads x head_dim,
+ * token stride q_token_stride elements) is rotated by positions[t] into
+ * q_out[t]; every head of k[t] is rotated and written, with v[t] unchanged,
+ * to pool slot slot_mapping[t] exactly as pkv_store_kvcache does (a negative
+ * slot skips the K/V write but still rotates q; a slot >= num_blocks *
+ * block_size is recorded as PKV_DEVERR_SLOT with info = t and skipped).
+ * The angle is reduced modulo 2 pi exactly, in 64-bit fixed-point turns (error
+ * below 1e-6 rad even at |position| = 2^31); sine and cosine come from the
+ * hardware approximation (within 4e-7 absolute on [-pi, pi]), the rotation
+ * runs in fp32, and each result is rounded once to bf16.
+ *
+ * q and q_out are both NULL (rotate and store K only) or both non-NULL;
+ * q_out may equal q (in place, equal strides) but must not partly overlap it
+ * or any other argument.  Supported: head_dim a multiple of 16 up to 256,
+ * token strides multiples of 8 elements, 16-byte aligned pointers; otherwise
+ * PKV_ERR_UNSUPPORTED.  rope_base must be positive and finite.
+ */
+PKV_API pkv_status pkv_rope_store_kvcache(const pkv_bf16 *q, int64_t q_token_stride, pkv_bf16 *q_out,
+                                  int64_t q_out_token_stride, const pkv_bf16 *k, int64_t k_token_stride,
+                                  const pkv_bf16 *v, int64_t v_token_stride, const int32_t *positions,
+                                  int64_t n_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, double rope_base, const int32_t *slot_mapping,
+                                  pkv_bf16 *k_cache, pkv_bf16 *v_cache, int32_t num_blocks,
+                                  int32_t block_size, pkv_stream_t stream);
 
 /*
  * a3. Varlen prefill attention over the paged cache.

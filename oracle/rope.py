@@ -30,20 +30,20 @@ def rotate_pair(a: float, b: float, angle: float):
 
 
 def rope(x, positions, base: float) -> np.ndarray:
-    """x: [N, H, d]; positions: [N].  Returns the rotated copy in float64."""
+    """x: [N, H, d]; positions: [N].  Returns the rotated copy in float64.
+
+    Angle of pair i at position p: p * base^(-2i/d); the rotation is
+    ``rotate_pair`` applied to (x[..., i], x[..., i + d/2]) for every token and
+    head at once."""
     x = np.asarray(x, dtype=np.float64)
-    n_tok, n_head, d = x.shape
+    d = x.shape[-1]
     half = d // 2
-    out = np.array(x, copy=True)
-    for t in range(n_tok):
-        pos = float(positions[t])
-        for i in range(half):
-            angle = pos * base ** (-2.0 * i / d)
-            for h in range(n_head):
-                a, b = rotate_pair(x[t, h, i], x[t, h, i + half], angle)
-                out[t, h, i] = a
-                out[t, h, i + half] = b
-    return out
+    inv_freq = np.array([base ** (-2.0 * i / d) for i in range(half)])
+    angle = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]   # [N, d/2]
+    c = np.cos(angle)[:, None, :]
+    s = np.sin(angle)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
 
 
 def rope_store_kvcache(q, k_cache, v_cache, k, v, positions, slots, block_size: int, base: float):

@@ -30,7 +30,7 @@ __all__ = [
     "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
     "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
     "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error",
-    "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "pkv_sample_dev", "DEVERR",
+    "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "pkv_sample_dev", "pkv_rope_store_kvcache", "DEVERR",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +73,10 @@ def load() -> ctypes.CDLL:
                                             _c_int32, _c_int32, _c_ptr, _c_ptr]),
         "pkv_store_kvcache": (ctypes.c_int, [_c_ptr, _c_ptr, _c_int64, _c_int64, _c_int64, _c_ptr, _c_ptr,
                                              _c_ptr, _c_int32, _c_int32, _c_int32, _c_int32, _c_ptr]),
+        "pkv_rope_store_kvcache": (ctypes.c_int, [_c_ptr, _c_int64, _c_ptr, _c_int64, _c_ptr, _c_int64, _c_ptr,
+                                                  _c_int64, _c_ptr, _c_int64, _c_int32, _c_int32, _c_int32,
+                                                  ctypes.c_double, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_int32,
+                                                  _c_ptr]),
         "pkv_prefill_workspace_size": (_c_size, [_c_int32] * 5),
         "pkv_prefill_varlen": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_int32,
                                               _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
@@ -184,6 +188,48 @@ def pkv_store_kvcache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
     _raise(load().pkv_store_kvcache(_ptr(k), _ptr(v), n, k.stride(0), v.stride(0), _ptr(slot_mapping),
                                     _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, _stream(stream)),
            "pkv_store_kvcache")
+
+
+def pkv_rope_store_kvcache(q: Optional[torch.Tensor], k: torch.Tensor, v: torch.Tensor, positions: torch.Tensor,
+                           slot_mapping: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           rope_base: float, q_out: Optional[torch.Tensor] = None,
+                           stream=None) -> Optional[torch.Tensor]:
+    """Rotate q and k by `positions` (rotary embedding), write rotated k and plain v to the pool.
+
+    Returns the rotated q (a new tensor, or `q_out`; pass ``q_out=q`` to rotate in place)."""
+    nb, bs, hkv, d = _pool_shape(k_cache)
+    _check(v_cache, "v_cache", torch.bfloat16, 4)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    for name, t in (("k", k), ("v", v)):
+        _check(t, name, torch.bfloat16, 3, contiguous=False)
+        if tuple(t.shape[1:]) != (hkv, d) or t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must be [n, {hkv}, {d}] with contiguous rows")
+    _check(positions, "positions", torch.int32, 1)
+    _check(slot_mapping, "slot_mapping", torch.int32, 1)
+    n = k.shape[0]
+    if v.shape[0] != n or slot_mapping.shape[0] != n or positions.shape[0] != n:
+        raise ValueError("k, v, positions and slot_mapping disagree on the token count")
+    hq = 0
+    if q is not None:
+        _check(q, "q", torch.bfloat16, 3, contiguous=False)
+        hq = q.shape[1]
+        if q.shape[0] != n or q.shape[2] != d or q.stride(2) != 1 or q.stride(1) != d:
+            raise ValueError(f"q must be [n, Hq, {d}] with contiguous rows")
+        if q_out is None:
+            q_out = torch.empty(n, hq, d, dtype=torch.bfloat16, device=q.device)
+        _check(q_out, "q_out", torch.bfloat16, 3, contiguous=False)
+        if tuple(q_out.shape) != tuple(q.shape) or q_out.stride(2) != 1 or q_out.stride(1) != d:
+            raise ValueError("q_out must match q's shape with contiguous rows")
+    elif q_out is not None:
+        raise ValueError("q_out given without q")
+    _raise(load().pkv_rope_store_kvcache(_ptr(q), q.stride(0) if q is not None else 0, _ptr(q_out),
+                                         q_out.stride(0) if q_out is not None else 0, _ptr(k), k.stride(0),
+                                         _ptr(v), v.stride(0), _ptr(positions), n, hq, hkv, d, float(rope_base),
+                                         _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb, bs,
+                                         _stream(stream)),
+           "pkv_rope_store_kvcache")
+    return q_out
 
 
 def pkv_prefill_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,

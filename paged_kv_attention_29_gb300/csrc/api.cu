@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <math.h>
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -150,6 +151,62 @@ pkv_status pkv_store_kvcache(const pkv_bf16* k, const pkv_bf16* v, int64_t n_tok
                                                k_cache, v_cache, static_cast<int64_t>(num_blocks) * block_size,
                                                static_cast<int>(row), err, as_stream(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_rope_store_kvcache(const pkv_bf16* q, int64_t q_token_stride, pkv_bf16* q_out,
+                                  int64_t q_out_token_stride, const pkv_bf16* k, int64_t k_token_stride,
+                                  const pkv_bf16* v, int64_t v_token_stride, const int32_t* positions,
+                                  int64_t n_tokens, int32_t num_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, double rope_base, const int32_t* slot_mapping,
+                                  pkv_bf16* k_cache, pkv_bf16* v_cache, int32_t num_blocks,
+                                  int32_t block_size, pkv_stream_t stream) {
+    if (n_tokens < 0 || num_heads < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+        block_size <= 0 || !(rope_base > 0.0) || rope_base == INFINITY)
+        return PKV_ERR_INVALID_ARG;
+    if ((q == nullptr) != (q_out == nullptr) || (q != nullptr && num_heads == 0)) return PKV_ERR_INVALID_ARG;
+    if (head_dim % 16 || head_dim > 2 * kMaxRopePairs) return PKV_ERR_UNSUPPORTED;
+    const int64_t kv_row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    const int64_t q_row = static_cast<int64_t>(num_heads) * head_dim;
+    if (k_token_stride < kv_row || v_token_stride < kv_row) return PKV_ERR_INVALID_ARG;
+    if (q && (q_token_stride < q_row || q_out_token_stride < q_row)) return PKV_ERR_INVALID_ARG;
+    if (q && q == q_out && q_token_stride != q_out_token_stride) return PKV_ERR_INVALID_ARG;
+    if (n_tokens == 0) return PKV_OK;
+    if (!k || !v || !positions || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (k_token_stride % 8 || v_token_stride % 8 || (q && (q_token_stride % 8 || q_out_token_stride % 8)))
+        return PKV_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(q_out) | reinterpret_cast<uintptr_t>(k) |
+         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(k_cache) |
+         reinterpret_cast<uintptr_t>(v_cache)) & 15)
+        return PKV_ERR_UNSUPPORTED;
+    if (n_tokens > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+    RopeStoreArgs a{};
+    a.q = q;
+    a.q_out = q_out;
+    a.k = k;
+    a.v = v;
+    a.positions = positions;
+    a.slots = slot_mapping;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.q_stride = q_token_stride;
+    a.q_out_stride = q_out_token_stride;
+    a.k_stride = k_token_stride;
+    a.v_stride = v_token_stride;
+    a.num_slots = static_cast<int64_t>(num_blocks) * block_size;
+    a.kv_row = kv_row;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    // pair i advances base^(-2i/d) radians per position: store the fraction of a
+    // turn in 64-bit fixed point (whole turns change no angle)
+    for (int i = 0; i < head_dim / 2; ++i) {
+        const double t = pow(rope_base, -2.0 * i / head_dim) / 6.283185307179586;
+        a.turns[i] = static_cast<uint64_t>(ldexp(t - floor(t), 64));   // t - floor(t) < 1: in range
+    }
+    if (rope_store_threads(a) == 0) return PKV_ERR_UNSUPPORTED;
+    int* err = device_error_word();
+    if (!err) return PKV_ERR_CUDA;
+    return launch_rope_store(a, n_tokens, err, as_stream(stream)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,

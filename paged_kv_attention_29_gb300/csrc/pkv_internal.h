@@ -36,6 +36,29 @@ cudaError_t launch_store_kvcache(const uint16_t* k, const uint16_t* v, int64_t n
                                  uint16_t* k_cache, uint16_t* v_cache, int64_t num_slots,
                                  int row_elems, int* err, cudaStream_t stream);
 
+// ---- f2: RoPE fused into the KV write -------------------------------------------
+constexpr int kMaxRopePairs = 128;   // head_dim <= 256
+
+struct RopeStoreArgs {
+    const uint16_t* q;        // nullptr: rotate and store K only
+    uint16_t* q_out;
+    const uint16_t* k;
+    const uint16_t* v;
+    const int32_t* positions;
+    const int32_t* slots;
+    uint16_t* k_cache;
+    uint16_t* v_cache;
+    int64_t q_stride, q_out_stride, k_stride, v_stride;   // elements between tokens
+    int64_t num_slots;
+    int64_t kv_row;            // num_kv_heads * head_dim
+    int num_heads, num_kv_heads, head_dim;
+    uint64_t turns[kMaxRopePairs];    // 2^64 * frac(base^(-2i/d) / (2 pi)), i < d/2
+};
+
+// Threads one CTA needs (one per work item of a token); 0 if above 1024.
+int rope_store_threads(const RopeStoreArgs& a);
+cudaError_t launch_rope_store(const RopeStoreArgs& a, int64_t n_tokens, int* err, cudaStream_t stream);
+
 // ---- a4 ---------------------------------------------------------------------
 struct DecodeArgs {
     const uint16_t* q;

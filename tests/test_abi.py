@@ -66,6 +66,14 @@ def test_host_argument_checks_return_before_launch(lib):
     # sample: row stride below vocab, empty vocab
     assert lib.pkv_sample(P, 2, 100, 50, P, 0, 0, P, P) == 1
     assert lib.pkv_sample(P, 2, 0, 0, P, 0, 0, P, P) == 1
+    # rope+store: head_dim not a multiple of 16; q without q_out; base <= 0; strides below a row
+    assert lib.pkv_rope_store_kvcache(P, 0, P, 0, P, 800, P, 800, P, 4, 0, 8, 100, 1e6, P, P, P, 4, 256, P) == 2
+    fake_q = ctypes.c_void_p(16)    # non-null, never dereferenced: the check returns first
+    assert lib.pkv_rope_store_kvcache(fake_q, 2048, P, 2048, P, 1024, P, 1024, P, 4, 16, 8, 128, 1e6,
+                                      P, P, P, 4, 256, P) == 1
+    assert lib.pkv_rope_store_kvcache(P, 0, P, 0, P, 1024, P, 1024, P, 4, 0, 8, 128, 0.0, P, P, P, 4, 256, P) == 1
+    assert lib.pkv_rope_store_kvcache(P, 0, P, 0, P, 512, P, 1024, P, 4, 0, 8, 128, 1e6, P, P, P, 4, 256, P) == 1
+    assert lib.pkv_rope_store_kvcache(P, 0, P, 0, P, 1024, P, 1024, P, 0, 0, 8, 128, 1e6, P, P, P, 4, 256, P) == 0
     # zero-size calls are no-ops
     assert lib.pkv_store_kvcache(P, P, 0, 1024, 1024, P, P, P, 4, 256, 8, 128, P) == 0
     assert lib.pkv_sample(P, 0, 10, 10, P, 0, 0, P, P) == 0

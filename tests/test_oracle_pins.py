@@ -406,3 +406,12 @@ def test_rope_store_rotates_q_and_k_not_v():
     np.testing.assert_array_equal(vc2[1, 2], v[1])
     np.testing.assert_allclose(kc2[1, 2], rp.rope(k, [3, 5], 1e4)[1], atol=1e-15)
     np.testing.assert_allclose(qr, rp.rope(q, [3, 5], 1e4), atol=1e-15)
+
+
+def test_rope_pairing_and_frequencies_closed_form():
+    """d = 4, base = 100: pair 0 = elements (0, 2) at frequency 1, pair 1 = elements (1, 3) at
+    frequency 100^(-2/4) = 0.1.  Catches an interleaved pairing or a wrong exponent."""
+    for p in (0.0, 1.0, 3.0, 250.0):
+        out = rp.rope(np.array([[[1.0, 1.0, 0.0, 0.0]]]), [p], base=100.0)[0, 0]
+        np.testing.assert_allclose(out, [math.cos(p), math.cos(0.1 * p), math.sin(p), math.sin(0.1 * p)],
+                                   rtol=0, atol=1e-13)
