@@ -71,18 +71,28 @@ constexpr int SM_V = SM_K + 2 * TILE_BYTES;       // 2 stages
 constexpr int SM_STAGE = SM_V + 2 * TILE_BYTES;   // epilogue staging: 4 KiB per softmax warp
 constexpr int STAGE_WARP_BYTES = 32 * 128;
 constexpr int SM_BAR = SM_STAGE + 8 * STAGE_WARP_BYTES;
+constexpr int RING = 4;                           // unit ring: producer -> MMA and softmax warps
 enum {
     BAR_QF = 0, BAR_QE, BAR_KF, BAR_KF1, BAR_KE, BAR_KE1, BAR_VF, BAR_VF1, BAR_VE, BAR_VE1,
-    BAR_SF, BAR_SF1, BAR_PF, BAR_PF1, BAR_OF, BAR_OF1, BAR_OE, BAR_OE1, BAR_DRAIN, NUM_BARS
+    BAR_SF, BAR_SF1, BAR_PF, BAR_PF1, BAR_OF, BAR_OF1, BAR_OE, BAR_OE1, BAR_DRAIN,
+    BAR_UF, BAR_UE = BAR_UF + RING, NUM_BARS = BAR_UE + RING
 };
-constexpr int SM_MISC = SM_BAR + NUM_BARS * 8;    // [0] TMEM base, [1] abort flag
+constexpr int RING_READERS = 1 + 8;               // the MMA thread and one lane of each softmax warp
+constexpr int SM_RING = (SM_BAR + NUM_BARS * 8 + 31) & ~31;   // RING x {idx, record}: 16-byte fields
+constexpr int SM_MISC = SM_RING + RING * 32;      // [0] TMEM base, [1] abort flag
 constexpr int SMEM_BYTES = SM_MISC + 16 + 1024;
+static_assert(SM_QA % 1024 == 0 && SM_QB % 1024 == 0 && SM_K % 1024 == 0 && SM_V % 1024 == 0,
+              "128B-swizzled operand tiles need 1024-byte alignment");
+static_assert(SM_STAGE % 16 == 0 && SM_BAR % 8 == 0 && SM_RING % 16 == 0 && SM_MISC % 16 == 0,
+              "vector, barrier and ring fields need their natural alignment");
 
 struct Params {
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* block_tables;
-    const uint4* plan;        // [0].x = number of (seq, pair) records; then {seq << 16 | pair, q_start, q_len, k_len}
+    const uint4* plan;        // [0].x = number of (seq, pair) records, [0].y = unit counter;
+                              // then {seq << 16 | pair, q_start, q_len, k_len}, most KV tiles first
+    unsigned int* next_unit;  // &plan[0].y: units are taken in list order by atomic increments
     uint16_t* out;
     int max_blocks;
     int num_heads;
@@ -159,13 +169,23 @@ __device__ __forceinline__ Unit unit_from(const Params& p, int idx, uint4 rec) {
     return u;
 }
 
-// Index of this CTA's r-th unit in the cost-sorted list (snake order), or -1.
-__device__ __forceinline__ int unit_index(int r, int total) {
-    const int G_ = static_cast<int>(gridDim.x);
-    const int c = static_cast<int>(blockIdx.x);
-    const int idx = r * G_ + ((r & 1) ? (G_ - 1 - c) : c);
+// Next unit of the cost-sorted list for this CTA, or -1: CTAs take units in
+// list order as they free up (longest first, so the last units to start are
+// the shortest and the CTAs finish close together).
+__device__ __forceinline__ int grab_unit(const Params& p, int total) {
+    const int idx = static_cast<int>(atomicAdd(p.next_unit, 1u));
     return idx < total ? idx : -1;
 }
+
+// The producer hands every unit (index and record) to the MMA thread and the
+// softmax warps through a ring in shared memory: slot r % RING, "full" barrier
+// (one arrival) and "empty" barrier (RING_READERS arrivals).
+struct alignas(16) RingEntry {
+    int idx;
+    int pad[3];
+    uint4 rec;
+};
+static_assert(sizeof(RingEntry) == 32, "ring slots are 32 bytes");
 
 // -------------------------------------------------------------------------
 // plan: (seq, pair) entries sorted by cost, most KV tiles first
@@ -231,6 +251,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t bars = base + SM_BAR;
     auto bar = [&](int i) { return bars + 8u * i; };
     uint32_t* misc = reinterpret_cast<uint32_t*>(gbase + SM_MISC);
+    RingEntry* ring = reinterpret_cast<RingEntry*>(gbase + SM_RING);
     Ctl ctl{reinterpret_cast<volatile uint32_t*>(misc + 1), p.err};
 
     const int tid = threadIdx.x;
@@ -240,7 +261,8 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (tid == 0) {
         for (int i = 0; i < NUM_BARS; ++i) {
             const bool softmax_arrive = (i == BAR_PF || i == BAR_PF1 || i == BAR_OE || i == BAR_OE1);
-            mbar_init(bar(i), softmax_arrive ? ROWS : 1);
+            const bool ring_empty = i >= BAR_UE && i < BAR_UE + RING;
+            mbar_init(bar(i), softmax_arrive ? ROWS : ring_empty ? RING_READERS : 1);
         }
         misc[1] = 0u;
         fence_barrier_init();
@@ -260,7 +282,8 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = misc[0];
     // everything above overlaps the plan kernel; global reads start here
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int total_units = static_cast<int>(__ldg(p.plan).x) * p.num_kv_heads;
+    const int total_units = static_cast<int>(*reinterpret_cast<const volatile unsigned int*>(p.plan)) *
+                            p.num_kv_heads;
 
     // Each warpgroup runs its own branch to the kernel's end (no common tail, so
     // every instruction has one register budget); every branch ends at the same
@@ -271,12 +294,19 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) {
             int t = 0;           // KV tiles issued by this CTA
             int issued_k = 0, issued_v = 0, uq = 0;
-            int idx = unit_index(0, total_units);
-            uint4 rec = unit_record(p, idx);
-            for (int r = 0; idx >= 0; ++r) {
+            int idx_next = grab_unit(p, total_units);
+            uint4 rec_next = unit_record(p, idx_next);
+            for (int r = 0;; ++r) {
+                const int idx = idx_next;
+                const uint4 rec = rec_next;
+                const int slot = r % RING;
+                if (r >= RING && !wait_phase(ctl, bar(BAR_UE + slot), ((r / RING) - 1) & 1)) break;
+                ring[slot].idx = idx;
+                ring[slot].rec = rec;
+                mbar_arrive(bar(BAR_UF + slot));       // release: the entry is visible to the waiters
+                if (idx < 0) break;
+                idx_next = grab_unit(p, total_units);  // its record is loaded once the first tile is issued
                 const Unit u = unit_from(p, idx, rec);
-                idx = unit_index(r + 1, total_units);
-                rec = unit_record(p, idx);            // in flight while this unit is issued
                 const int n = max(u.n[0], u.n[1]);
                 if (uq >= 1 && !wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1)) break;
                 const int qrow = u.q_start + u.pair * UNIT_TOK;
@@ -307,6 +337,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tma_load_4d(sV + st * TILE_BYTES, &tm_v, bar(BAR_VF + st), 0, u.g, off, phys);
                     tma_load_4d(sV + st * TILE_BYTES + HALF_BYTES, &tm_v, bar(BAR_VF + st), 64, u.g, off, phys);
                     ++issued_v;
+                    if (j == 0) rec_next = unit_record(p, idx_next);
                 }
                 if (!ok) break;
             }
@@ -346,12 +377,14 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mma_commit(bar(BAR_SF + X));
                 if (--s_left == 0) mma_commit(bar(BAR_QE));   // the unit's Q tiles are no longer read
             };
-            int idx = unit_index(0, total_units);
-            uint4 rec = unit_record(p, idx);
-            for (int r = 0; ok && idx >= 0; ++r) {
+            for (int r = 0; ok; ++r) {
+                const int slot = r % RING;
+                if (!(ok = wait_phase(ctl, bar(BAR_UF + slot), (r / RING) & 1))) break;
+                const int idx = ring[slot].idx;
+                const uint4 rec = ring[slot].rec;
+                mbar_arrive(bar(BAR_UE + slot));
+                if (idx < 0) break;
                 const Unit u = unit_from(p, idx, rec);
-                idx = unit_index(r + 1, total_units);
-                rec = unit_record(p, idx);
                 const int n = max(u.n[0], u.n[1]);
                 s_left = u.n[0] + u.n[1];
                 if (!(ok = wait_phase(ctl, bar(BAR_QF), uq & 1))) break;
@@ -440,16 +473,18 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const float sc = p.scale_log2;
         int cntS = 0, uact = 0;
         bool ok = true;
-        int idx = unit_index(0, total_units);
-        uint4 rec = unit_record(p, idx);
-        for (int r = 0; ok && idx >= 0; ++r) {
+        for (int r = 0; ok; ++r) {
+            const int slot = r % RING;
+            ok = __all_sync(0xffffffffu, wait_phase(ctl, bar(BAR_UF + slot), (r / RING) & 1));
+            if (!ok) break;
+            const int idx = ring[slot].idx;
+            const uint4 rec = ring[slot].rec;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_UE + slot));
+            if (idx < 0) break;
             const Unit u = unit_from(p, idx, rec);
-            idx = unit_index(r + 1, total_units);
             const int nx = X ? u.n[1] : u.n[0];
-            if (nx == 0) {
-                rec = unit_record(p, idx);
-                continue;
-            }
+            if (nx == 0) continue;
             const int qi = u.pair * UNIT_TOK + X * QTOK + ti;
             const int jmax = min(qi + u.offset, u.kl - 1);
             float m_used = -INFINITY, l = 0.f;
@@ -532,7 +567,6 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!ok) break;
             ++uact;
             tc_fence_after();
-            rec = unit_record(p, idx);   // the next unit's record loads while this epilogue runs
             // O / l -> bf16, 64 columns at a time: each thread writes its row into this warp's
             // staging area (16-byte chunks XOR-swizzled by row, no bank conflicts), then the warp
             // stores four 128-byte row halves per instruction
@@ -629,6 +663,7 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     p.cu_k = a.cu_k;
     p.block_tables = a.block_tables;
     p.plan = static_cast<const uint4*>(a.workspace);
+    p.next_unit = static_cast<unsigned int*>(a.workspace) + 1;
     p.out = a.out;
     p.max_blocks = a.max_blocks;
     p.num_heads = a.num_heads;
