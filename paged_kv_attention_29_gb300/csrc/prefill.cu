@@ -73,8 +73,7 @@ constexpr int STAGE_WARP_BYTES = 32 * 128;
 constexpr int SM_BAR = SM_STAGE + 8 * STAGE_WARP_BYTES;
 constexpr int RING = 4;                           // unit ring: producer -> MMA and softmax warps
 enum {
-    BAR_QF = 0, BAR_QE, BAR_KF, BAR_KF1, BAR_KE, BAR_KE1, BAR_VF, BAR_VF1, BAR_VE, BAR_VE1,
-    BAR_SF, BAR_SF1, BAR_PF, BAR_PF1, BAR_OF, BAR_OF1, BAR_OE, BAR_OE1, BAR_DRAIN,
+    BAR_QF = 0, BAR_QE, BAR_GF, BAR_GF1, BAR_GE, BAR_GE1, BAR_SF, BAR_SF1, BAR_PF, BAR_PF1, BAR_OF, BAR_OF1, BAR_OE, BAR_OE1, BAR_DRAIN,
     BAR_UF, BAR_UE = BAR_UF + RING, NUM_BARS = BAR_UE + RING
 };
 constexpr int RING_READERS = 1 + 8;               // the MMA thread and one lane of each softmax warp
@@ -292,23 +291,42 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         regs_dec<kControlRegs>();
         // ---------------------------------------------------------------- TMA
         if (lane == 0) {
-            int t = 0;           // KV tiles issued by this CTA
-            int issued_k = 0, issued_v = 0, uq = 0;
-            int idx_next = grab_unit(p, total_units);
-            uint4 rec_next = unit_record(p, idx_next);
+            int uq = 0, groups = 0;   // Q tiles and K/V groups issued
+            // a tile's K or V: TMA from the physical block the table names (128 keys, two 64-dim halves)
+            auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t b, const Unit& w, int jj) {
+                const int key0 = jj * KT;
+                const int lb = key0 / p.block_size;
+                const int phys = __ldg(p.block_tables + static_cast<int64_t>(w.seq) * p.max_blocks + lb);
+                if (phys < 0 || phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, w.seq);
+                const int off = key0 - lb * p.block_size;
+                tma_load_4d(dst, map, b, 0, w.g, off, phys);
+                tma_load_4d(dst + HALF_BYTES, map, b, 64, w.g, off, phys);
+            };
+            // two units of lookahead: the current one, and the next, whose first K tile rides in
+            // the current unit's last group
+            int idx_cur = grab_unit(p, total_units);
+            uint4 rec_cur = unit_record(p, idx_cur);
+            int idx_nxt = grab_unit(p, total_units);
+            uint4 rec_nxt = unit_record(p, idx_nxt);
+            bool ok = true;
+            if (idx_cur >= 0) {                       // group 0: the first unit's first K tile
+                mbar_arrive_expect_tx(bar(BAR_GF), TILE_BYTES);
+                load_tile(&tm_k, sK, bar(BAR_GF), unit_from(p, idx_cur, rec_cur), 0);
+                groups = 1;
+            }
+            int t = 0;                                // tiles of the units before the current one
             for (int r = 0;; ++r) {
-                const int idx = idx_next;
-                const uint4 rec = rec_next;
                 const int slot = r % RING;
-                if (r >= RING && !wait_phase(ctl, bar(BAR_UE + slot), ((r / RING) - 1) & 1)) break;
-                ring[slot].idx = idx;
-                ring[slot].rec = rec;
-                mbar_arrive(bar(BAR_UF + slot));       // release: the entry is visible to the waiters
-                if (idx < 0) break;
-                idx_next = grab_unit(p, total_units);  // its record is loaded once the first tile is issued
-                const Unit u = unit_from(p, idx, rec);
+                if (r >= RING && !(ok = wait_phase(ctl, bar(BAR_UE + slot), ((r / RING) - 1) & 1))) break;
+                ring[slot].idx = idx_cur;
+                ring[slot].rec = rec_cur;
+                mbar_arrive(bar(BAR_UF + slot));     // release: the entry is visible to the waiters
+                if (idx_cur < 0) break;
+                const int idx_n2 = grab_unit(p, total_units);   // its record loads after the first group
+                uint4 rec_n2 = make_uint4(0u, 0u, 0u, 0u);
+                const Unit u = unit_from(p, idx_cur, rec_cur);
                 const int n = max(u.n[0], u.n[1]);
-                if (uq >= 1 && !wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1)) break;
+                if (uq >= 1 && !(ok = wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1))) break;
                 const int qrow = u.q_start + u.pair * UNIT_TOK;
                 mbar_arrive_expect_tx(bar(BAR_QF), u.n[1] > 0 ? 2 * TILE_BYTES : TILE_BYTES);
                 tma_load_3d(sQ[0], &tm_q, bar(BAR_QF), 0, G * u.g, qrow);
@@ -318,34 +336,32 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tma_load_3d(sQ[1] + HALF_BYTES, &tm_q, bar(BAR_QF), 64, G * u.g, qrow + QTOK);
                 }
                 ++uq;
-                const int32_t* bt = p.block_tables + static_cast<int64_t>(u.seq) * p.max_blocks;
-                bool ok = true;
-                for (int j = 0; j < n; ++j, ++t) {
-                    const int st = t & 1;
-                    const int key0 = j * KT;
-                    const int lb = key0 / p.block_size;
-                    const int phys = __ldg(bt + lb);
-                    if (phys < 0 || phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, u.seq);
-                    const int off = key0 - lb * p.block_size;
-                    if (t >= 2 && !(ok = wait_phase(ctl, bar(BAR_KE + st), ((t >> 1) - 1) & 1))) break;
-                    mbar_arrive_expect_tx(bar(BAR_KF + st), TILE_BYTES);
-                    tma_load_4d(sK + st * TILE_BYTES, &tm_k, bar(BAR_KF + st), 0, u.g, off, phys);
-                    tma_load_4d(sK + st * TILE_BYTES + HALF_BYTES, &tm_k, bar(BAR_KF + st), 64, u.g, off, phys);
-                    ++issued_k;
-                    if (t >= 2 && !(ok = wait_phase(ctl, bar(BAR_VE + st), ((t >> 1) - 1) & 1))) break;
-                    mbar_arrive_expect_tx(bar(BAR_VF + st), TILE_BYTES);
-                    tma_load_4d(sV + st * TILE_BYTES, &tm_v, bar(BAR_VF + st), 0, u.g, off, phys);
-                    tma_load_4d(sV + st * TILE_BYTES + HALF_BYTES, &tm_v, bar(BAR_VF + st), 64, u.g, off, phys);
-                    ++issued_v;
-                    if (j == 0) rec_next = unit_record(p, idx_next);
+                for (int j = 0; j < n; ++j) {
+                    // group gu = tile + 1: V of this tile (V stage tile & 1) and K of the tile after it
+                    // (K stage gu & 1); it reuses the stages of group gu - 2
+                    const int gu = t + j + 1;
+                    const int sg = gu & 1;
+                    if (gu >= 2 && !(ok = wait_phase(ctl, bar(BAR_GE + sg), ((gu - 2) >> 1) & 1))) break;
+                    const bool k_here = j + 1 < n;
+                    const bool k_next = !k_here && idx_nxt >= 0;
+                    mbar_arrive_expect_tx(bar(BAR_GF + sg), (k_here || k_next) ? 2 * TILE_BYTES : TILE_BYTES);
+                    load_tile(&tm_v, sV + (sg ^ 1) * TILE_BYTES, bar(BAR_GF + sg), u, j);
+                    if (k_here) load_tile(&tm_k, sK + sg * TILE_BYTES, bar(BAR_GF + sg), u, j + 1);
+                    else if (k_next) load_tile(&tm_k, sK + sg * TILE_BYTES, bar(BAR_GF + sg), unit_from(p, idx_nxt, rec_nxt), 0);
+                    ++groups;
+                    if (j == 0) rec_n2 = unit_record(p, idx_n2);
                 }
                 if (!ok) break;
+                t += n;
+                idx_cur = idx_nxt;
+                rec_cur = rec_nxt;
+                idx_nxt = idx_n2;
+                rec_nxt = rec_n2;
             }
             if (*ctl.abort) {
                 // copies already issued must land before shared memory is released
                 if (uq > 0) wait_drain(bar(BAR_QF), (uq - 1) & 1);
-                for (int k = max(0, issued_k - 2); k < issued_k; ++k) wait_drain(bar(BAR_KF + (k & 1)), (k >> 1) & 1);
-                for (int k = max(0, issued_v - 2); k < issued_v; ++k) wait_drain(bar(BAR_VF + (k & 1)), (k >> 1) & 1);
+                for (int g = max(0, groups - 2); g < groups; ++g) wait_drain(bar(BAR_GF + (g & 1)), (g >> 1) & 1);
             }
         }
         __syncwarp();
@@ -389,47 +405,52 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 s_left = u.n[0] + u.n[1];
                 if (!(ok = wait_phase(ctl, bar(BAR_QF), uq & 1))) break;
                 ++uq;
-                if (!(ok = wait_phase(ctl, bar(BAR_KF + (t & 1)), (t >> 1) & 1))) break;
+                // group t holds this unit's first K; only group 0 is not waited in a previous unit
+                if (t == 0 && !(ok = wait_phase(ctl, bar(BAR_GF), 0))) break;
                 tc_fence_after();
                 issue_s(0, t & 1);
                 if (u.n[1] > 0) issue_s(1, t & 1);
-                mma_commit(bar(BAR_KE + (t & 1)));
+                mma_commit(bar(BAR_GE + (t & 1)));     // group t consumed: V(t-1) earlier, K(t) now
                 for (int j = 0; j < n && ok; ++j) {
                     const int tj = t + j;
-                    const int st = tj & 1;
-                    bool v_ready = false, k_next_ready = false, v_tail_done = false;
+                    const int st = tj & 1;                    // V stage of this tile
+                    const int sg = (tj + 1) & 1;              // its group: V(tj) and K(tj + 1)
                     const int keys_here = min(KT, u.kl - j * KT);
                     const int ksteps = (keys_here + 15) >> 4;
+                    const bool s_next = j + 1 < n;            // some tile still needs S(j+1)
+                    // Everything this step needs except P -- the group, and at a unit's first step the
+                    // previous unit's epilogue -- is taken here, while the tensor pipe still works
+                    // through the batch issued last, so after P lands only issuing remains.
+                    if (!(ok = wait_phase(ctl, bar(BAR_GF + sg), ((tj + 1) >> 1) & 1))) break;
+                    if (j == 0) {
+#pragma unroll
+                        for (int X = 0; X < 2; ++X)
+                            if (ok && u.n[X] > 0 && uact[X] >= 1)
+                                ok = wait_phase(ctl, bar(BAR_OE + X), (uact[X] - 1) & 1);
+                        if (!ok) break;
+                    }
+                    if (keys_here & 15) {
+                        // rows past the sequence's last key may hold anything (freed blocks are not
+                        // cleared); their P is zero but 0 * NaN is NaN, so clear them
+                        uint8_t* vt = gbase + SM_V + st * TILE_BYTES;
+                        for (int rr = keys_here; rr < ksteps * 16; ++rr) {
+                            uint4* r0 = reinterpret_cast<uint4*>(vt + rr * 128);
+                            uint4* r1 = reinterpret_cast<uint4*>(vt + HALF_BYTES + rr * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                r0[c] = make_uint4(0, 0, 0, 0);
+                                r1[c] = make_uint4(0, 0, 0, 0);
+                            }
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    const uint64_t dvs = st ? dv1 : dv0;
 #pragma unroll
                     for (int X = 0; X < 2; ++X) {
-                        if (!ok) break;
                         if (j < u.n[X]) {
                             if (!(ok = wait_phase(ctl, bar(BAR_PF + X), cntP[X] & 1))) break;
                             ++cntP[X];
-                            if (!v_ready) {
-                                if (!(ok = wait_phase(ctl, bar(BAR_VF + st), (tj >> 1) & 1))) break;
-                                v_ready = true;
-                            }
-                            if (j == 0 && uact[X] >= 1 && !(ok = wait_phase(ctl, bar(BAR_OE + X), (uact[X] - 1) & 1)))
-                                break;
                             tc_fence_after();
-                            if ((keys_here & 15) && !v_tail_done) {
-                                // rows past the sequence's last key may hold anything (freed blocks are not
-                                // cleared); their P is zero but 0 * NaN is NaN, so clear them
-                                uint8_t* vt = gbase + SM_V + st * TILE_BYTES;
-                                for (int rr = keys_here; rr < ksteps * 16; ++rr) {
-                                    uint4* r0 = reinterpret_cast<uint4*>(vt + rr * 128);
-                                    uint4* r1 = reinterpret_cast<uint4*>(vt + HALF_BYTES + rr * 128);
-#pragma unroll
-                                    for (int c = 0; c < 8; ++c) {
-                                        r0[c] = make_uint4(0, 0, 0, 0);
-                                        r1[c] = make_uint4(0, 0, 0, 0);
-                                    }
-                                }
-                                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                                v_tail_done = true;
-                            }
-                            const uint64_t dvs = st ? dv1 : dv0;
                             for (int ks = 0; ks < ksteps; ++ks)
                                 mma_ts(tmem + O_COL(X), tmem + S_COL(X) + ks * 8, dvs + ks * (16 * 128 >> 4),
                                        idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
@@ -439,17 +460,14 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             }
                         }
                         if (j + 1 < u.n[X]) {
-                            if (!k_next_ready) {
-                                if (!(ok = wait_phase(ctl, bar(BAR_KF + ((tj + 1) & 1)), ((tj + 1) >> 1) & 1))) break;
-                                tc_fence_after();
-                                k_next_ready = true;
-                            }
+                            tc_fence_after();
                             issue_s(X, (tj + 1) & 1);
                         }
                     }
                     if (!ok) break;
-                    mma_commit(bar(BAR_VE + st));
-                    if (j + 1 < n) mma_commit(bar(BAR_KE + ((tj + 1) & 1)));
+                    // the group is consumed once S(tj+1) is issued; on a unit's last tile its K belongs
+                    // to the next unit, whose start commits it
+                    if (s_next) mma_commit(bar(BAR_GE + sg));
                 }
                 t += n;
             }
