@@ -125,6 +125,12 @@ __device__ __forceinline__ bool wait_phase(const Ctl& c, uint32_t bar, uint32_t 
     }
 }
 
+// wait_phase for a warp that runs in step: every lane waits, and the result is
+// made warp-uniform.
+__device__ __forceinline__ bool wait_warp(const Ctl& c, uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait_phase(c, bar, parity));
+}
+
 __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait_sleep(bar, parity, 500000u))
@@ -370,7 +376,9 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else if (warp == MMA_WARP) {
         regs_dec<kControlRegs>();
         // ---------------------------------------------------------------- MMA
-        if (lane == 0) {
+        // The whole warp runs this loop in step; each tcgen05 instruction is issued by one
+        // elected lane, so descriptors and counters stay warp-uniform.
+        {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(ROWS, KT, 0, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(ROWS, D, 0, 1);
             int t = 0, uq = 0;
@@ -388,29 +396,31 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t koff = ((ks >> 2) * HALF_BYTES + (ks & 3) * 32) >> 4;
-                    mma_ss(tmem + S_COL(X), da + koff, db + koff, idesc_qk, ks > 0 ? 1u : 0u);
+                    mma_ss_warp(tmem + S_COL(X), da + koff, db + koff, idesc_qk, ks > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(BAR_SF + X));
-                if (--s_left == 0) mma_commit(bar(BAR_QE));   // the unit's Q tiles are no longer read
+                mma_commit_warp(bar(BAR_SF + X));
+                if (--s_left == 0) mma_commit_warp(bar(BAR_QE));   // the unit's Q tiles are no longer read
             };
             for (int r = 0; ok; ++r) {
                 const int slot = r % RING;
-                if (!(ok = wait_phase(ctl, bar(BAR_UF + slot), (r / RING) & 1))) break;
+                if (!(ok = wait_warp(ctl, bar(BAR_UF + slot), (r / RING) & 1))) break;
                 const int idx = ring[slot].idx;
                 const uint4 rec = ring[slot].rec;
-                mbar_arrive(bar(BAR_UE + slot));
+                __syncwarp();                          // every lane has read the entry
+                if (lane == 0) mbar_arrive(bar(BAR_UE + slot));
+                __syncwarp();
                 if (idx < 0) break;
                 const Unit u = unit_from(p, idx, rec);
                 const int n = max(u.n[0], u.n[1]);
                 s_left = u.n[0] + u.n[1];
-                if (!(ok = wait_phase(ctl, bar(BAR_QF), uq & 1))) break;
+                if (!(ok = wait_warp(ctl, bar(BAR_QF), uq & 1))) break;
                 ++uq;
                 // group t holds this unit's first K; only group 0 is not waited in a previous unit
-                if (t == 0 && !(ok = wait_phase(ctl, bar(BAR_GF), 0))) break;
+                if (t == 0 && !(ok = wait_warp(ctl, bar(BAR_GF), 0))) break;
                 tc_fence_after();
                 issue_s(0, t & 1);
                 if (u.n[1] > 0) issue_s(1, t & 1);
-                mma_commit(bar(BAR_GE + (t & 1)));     // group t consumed: V(t-1) earlier, K(t) now
+                mma_commit_warp(bar(BAR_GE + (t & 1)));     // group t consumed: V(t-1) earlier, K(t) now
                 for (int j = 0; j < n && ok; ++j) {
                     const int tj = t + j;
                     const int st = tj & 1;                    // V stage of this tile
@@ -421,41 +431,39 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     // Everything this step needs except P -- the group, and at a unit's first step the
                     // previous unit's epilogue -- is taken here, while the tensor pipe still works
                     // through the batch issued last, so after P lands only issuing remains.
-                    if (!(ok = wait_phase(ctl, bar(BAR_GF + sg), ((tj + 1) >> 1) & 1))) break;
+                    if (!(ok = wait_warp(ctl, bar(BAR_GF + sg), ((tj + 1) >> 1) & 1))) break;
                     if (j == 0) {
 #pragma unroll
                         for (int X = 0; X < 2; ++X)
                             if (ok && u.n[X] > 0 && uact[X] >= 1)
-                                ok = wait_phase(ctl, bar(BAR_OE + X), (uact[X] - 1) & 1);
+                                ok = wait_warp(ctl, bar(BAR_OE + X), (uact[X] - 1) & 1);
                         if (!ok) break;
                     }
                     if (keys_here & 15) {
                         // rows past the sequence's last key may hold anything (freed blocks are not
                         // cleared); their P is zero but 0 * NaN is NaN, so clear them
+                        // (16-byte chunks spread over the warp; each row is 2 halves x 8 chunks)
                         uint8_t* vt = gbase + SM_V + st * TILE_BYTES;
-                        for (int rr = keys_here; rr < ksteps * 16; ++rr) {
-                            uint4* r0 = reinterpret_cast<uint4*>(vt + rr * 128);
-                            uint4* r1 = reinterpret_cast<uint4*>(vt + HALF_BYTES + rr * 128);
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                r0[c] = make_uint4(0, 0, 0, 0);
-                                r1[c] = make_uint4(0, 0, 0, 0);
-                            }
+                        for (int i = lane; i < (ksteps * 16 - keys_here) * 16; i += 32) {
+                            const int rr = keys_here + (i >> 4);
+                            *reinterpret_cast<uint4*>(vt + ((i >> 3) & 1) * HALF_BYTES + rr * 128 + (i & 7) * 16) =
+                                make_uint4(0, 0, 0, 0);
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
                     }
                     const uint64_t dvs = st ? dv1 : dv0;
 #pragma unroll
                     for (int X = 0; X < 2; ++X) {
                         if (j < u.n[X]) {
-                            if (!(ok = wait_phase(ctl, bar(BAR_PF + X), cntP[X] & 1))) break;
+                            if (!(ok = wait_warp(ctl, bar(BAR_PF + X), cntP[X] & 1))) break;
                             ++cntP[X];
                             tc_fence_after();
                             for (int ks = 0; ks < ksteps; ++ks)
-                                mma_ts(tmem + O_COL(X), tmem + S_COL(X) + ks * 8, dvs + ks * (16 * 128 >> 4),
+                                mma_ts_warp(tmem + O_COL(X), tmem + S_COL(X) + ks * 8, dvs + ks * (16 * 128 >> 4),
                                        idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                             if (j == u.n[X] - 1) {
-                                mma_commit(bar(BAR_OF + X));
+                                mma_commit_warp(bar(BAR_OF + X));
                                 ++uact[X];
                             }
                         }
@@ -467,12 +475,13 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (!ok) break;
                     // the group is consumed once S(tj+1) is issued; on a unit's last tile its K belongs
                     // to the next unit, whose start commits it
-                    if (s_next) mma_commit(bar(BAR_GE + sg));
+                    if (s_next) mma_commit_warp(bar(BAR_GE + sg));
                 }
                 t += n;
             }
-            mma_commit(bar(BAR_DRAIN));
+            mma_commit_warp(bar(BAR_DRAIN));
             wait_drain(bar(BAR_DRAIN), 0);
+            __syncwarp();
         }
         __syncwarp();
         tc_fence_before();
