@@ -308,12 +308,11 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 tma_load_4d(dst, map, b, 0, w.g, off, phys);
                 tma_load_4d(dst + HALF_BYTES, map, b, 64, w.g, off, phys);
             };
-            // two units of lookahead: the current one, and the next, whose first K tile rides in
-            // the current unit's last group
+            // one unit of lookahead: the next unit is taken when the current one starts (its first K
+            // tile rides in the current unit's last group), so no CTA holds more than one unit it
+            // has not started
             int idx_cur = grab_unit(p, total_units);
             uint4 rec_cur = unit_record(p, idx_cur);
-            int idx_nxt = grab_unit(p, total_units);
-            uint4 rec_nxt = unit_record(p, idx_nxt);
             bool ok = true;
             if (idx_cur >= 0) {                       // group 0: the first unit's first K tile
                 mbar_arrive_expect_tx(bar(BAR_GF), TILE_BYTES);
@@ -328,8 +327,8 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ring[slot].rec = rec_cur;
                 mbar_arrive(bar(BAR_UF + slot));     // release: the entry is visible to the waiters
                 if (idx_cur < 0) break;
-                const int idx_n2 = grab_unit(p, total_units);   // its record loads after the first group
-                uint4 rec_n2 = make_uint4(0u, 0u, 0u, 0u);
+                const int idx_nxt = grab_unit(p, total_units);  // its record is read for the last group
+                uint4 rec_nxt = make_uint4(0u, 0u, 0u, 0u);
                 const Unit u = unit_from(p, idx_cur, rec_cur);
                 const int n = max(u.n[0], u.n[1]);
                 if (uq >= 1 && !(ok = wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1))) break;
@@ -350,19 +349,17 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (gu >= 2 && !(ok = wait_phase(ctl, bar(BAR_GE + sg), ((gu - 2) >> 1) & 1))) break;
                     const bool k_here = j + 1 < n;
                     const bool k_next = !k_here && idx_nxt >= 0;
+                    if (k_next) rec_nxt = unit_record(p, idx_nxt);
                     mbar_arrive_expect_tx(bar(BAR_GF + sg), (k_here || k_next) ? 2 * TILE_BYTES : TILE_BYTES);
                     load_tile(&tm_v, sV + (sg ^ 1) * TILE_BYTES, bar(BAR_GF + sg), u, j);
                     if (k_here) load_tile(&tm_k, sK + sg * TILE_BYTES, bar(BAR_GF + sg), u, j + 1);
                     else if (k_next) load_tile(&tm_k, sK + sg * TILE_BYTES, bar(BAR_GF + sg), unit_from(p, idx_nxt, rec_nxt), 0);
                     ++groups;
-                    if (j == 0) rec_n2 = unit_record(p, idx_n2);
                 }
                 if (!ok) break;
                 t += n;
                 idx_cur = idx_nxt;
-                rec_cur = rec_nxt;
-                idx_nxt = idx_n2;
-                rec_nxt = rec_n2;
+                rec_cur = idx_nxt >= 0 ? rec_nxt : make_uint4(0u, 0u, 0u, 0u);
             }
             if (*ctl.abort) {
                 // copies already issued must land before shared memory is released
