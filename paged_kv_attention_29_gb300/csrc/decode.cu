@@ -184,6 +184,8 @@ template <bool kFused>
 __global__ void __launch_bounds__(THREADS, 1)
 decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                      const Params p) {
+    // let the combine grid launch now; it waits for this grid's completion before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1 KiB-aligned base
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageRegion);
@@ -443,6 +445,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 // One warp per (sequence, query head): merge its pieces in warp order.
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the split-K grid's pieces are complete
     const int lane = threadIdx.x & 31;
     const int idx = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (idx >= p.batch * num_heads) return;
@@ -574,9 +577,20 @@ pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream) {
     else
         decode_splitk_kernel<false><<<W / WARPS, THREADS, smem, stream>>>(tm_k, tm_v, p);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    // the combine is launched as a programmatic dependent of the split-K grid: its CTAs are
+    // resident (waiting in griddepcontrol.wait) by the time the last split-K warp finishes
     const int n_rows = a.batch * a.num_heads;
-    decode_combine_kernel<<<(n_rows + 3) / 4, 128, 0, stream>>>(p, a.num_heads, a.out);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((n_rows + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_combine_kernel, p, a.num_heads, a.out) != cudaSuccess) return PKV_ERR_CUDA;
     return PKV_OK;
 }
 
