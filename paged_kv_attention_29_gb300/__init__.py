@@ -30,7 +30,7 @@ __all__ = [
     "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
     "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
     "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error",
-    "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "pkv_sample_dev", "pkv_rope_store_kvcache", "DEVERR",
+    "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "pkv_sample_dev", "pkv_rope_store_kvcache", "DecodeAppendCall", "DEVERR",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -339,6 +339,39 @@ def pkv_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
                                     _ptr(slot_mapping), _ptr(workspace), workspace.numel(), _stream(stream)),
            "pkv_decode_append")
     return out
+
+
+class DecodeAppendCall:
+    """pkv_decode_append on a fixed set of buffers, checked and marshalled once.
+
+    A serving loop calls the same step on the same buffers (inputs copied into
+    them) every iteration; this object does the argument checks and the ctypes
+    marshalling at construction, so each call is one C-ABI call.  The buffers
+    must stay alive and keep their shapes; their contents may change freely."""
+
+    def __init__(self, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                 softmax_scale, out, slot_mapping=None, workspace=None, stream=None):
+        # one validating call through the checked path (it also runs the step once)
+        pkv_decode_append(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                          softmax_scale, out=out, slot_mapping=slot_mapping, workspace=workspace, stream=stream)
+        nb, bs, hkv, d = _pool_shape(k_cache)
+        batch, hq, _ = q.shape
+        if workspace is None:
+            workspace = decode_workspace(batch, hq, hkv, d, q.device)
+        self._keep = (q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, slot_mapping, workspace)
+        self._fn = load().pkv_decode_append
+        self._args = (_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                      block_tables.shape[1], _ptr(context_lens), batch, int(max_context_len), hq, hkv, d, bs, nb,
+                      float(softmax_scale), _ptr(out), _ptr(slot_mapping), _ptr(workspace), workspace.numel())
+        self._stream = None if stream is None else _stream(stream)   # None: the current stream per call
+        self.out = out
+
+    def __call__(self, stream=None) -> torch.Tensor:
+        """Launch on `stream`, else on the stream given at construction, else on the current stream
+        (so a call made while a CUDA graph is being captured is captured)."""
+        s = _stream(stream) if stream is not None else (self._stream if self._stream is not None else _stream())
+        _raise(self._fn(*self._args, s), "pkv_decode_append")
+        return self.out
 
 
 def pkv_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,

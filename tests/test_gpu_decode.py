@@ -160,3 +160,29 @@ def test_decode_append_zero_context_writes_nothing(pkv):
     assert len(changed) == 2                                   # one row for each non-empty sequence
     assert torch.count_nonzero(out[1]).item() == 0 and torch.count_nonzero(out[3]).item() == 0
     expect_no_device_error(pkv)
+
+
+def test_prepared_decode_append_call(pkv):
+    """DecodeAppendCall: checked and marshalled once, then each call sees the buffers' current contents."""
+    wl = W.decode_b64(batch=16)
+    vals = W.paged_values(wl)
+    b = GpuBatch(wl, vals)
+    out = torch.empty_like(b.q)
+    call = pkv.DecodeAppendCall(b.q, b.k_new, b.v_new, b.k_cache, b.v_cache, b.block_tables, b.kv_lens,
+                                int(wl.kv_lens.max()), wl.softmax_scale, out=out)
+    ref = GpuBatch(wl, vals)
+    o_ref = pkv.pkv_decode_append(ref.q, ref.k_new, ref.v_new, ref.k_cache, ref.v_cache, ref.block_tables,
+                                  ref.kv_lens, int(wl.kv_lens.max()), wl.softmax_scale)
+    assert np.array_equal(bits(out), bits(o_ref))
+    # new inputs copied into the same buffers are picked up by the next call
+    g = torch.Generator().manual_seed(5)
+    q2 = torch.randn(tuple(b.q.shape), generator=g).to(torch.bfloat16).cuda()
+    b.q.copy_(q2)
+    ref.q.copy_(q2)
+    assert call() is out
+    o_ref2 = pkv.pkv_decode_append(ref.q, ref.k_new, ref.v_new, ref.k_cache, ref.v_cache, ref.block_tables,
+                                   ref.kv_lens, int(wl.kv_lens.max()), wl.softmax_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), bits(o_ref2))
+    assert not np.array_equal(bits(o_ref2), bits(o_ref))
+    expect_no_device_error(pkv)

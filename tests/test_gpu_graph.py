@@ -71,3 +71,28 @@ def test_sample_dev_equals_sample(pkv):
     b = pkv.pkv_sample(s_in.logits, s_in.temperatures, 12345, offset=77)
     assert torch.equal(a, b)
     expect_no_device_error(pkv)
+
+
+def test_prepared_call_made_before_capture_is_captured(pkv):
+    """A DecodeAppendCall built on the default stream and then called inside a capture must land in the
+    graph: after new q values are copied into its buffer, a replay must give the eager result for them."""
+    wl = W.decode_b64(batch=8, lo=100, hi=600)
+    v = W.paged_values(wl, device="cuda")
+    bt = torch.from_numpy(wl.block_tables).cuda()
+    ctx = torch.from_numpy(wl.kv_lens).cuda()
+    out = torch.empty_like(v.q)
+    call = pkv.DecodeAppendCall(v.q, v.k_new, v.v_new, v.k_cache, v.v_cache, bt, ctx, int(wl.kv_lens.max()),
+                                wl.softmax_scale, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    out.zero_()
+    gen = torch.Generator().manual_seed(77)
+    v.q.copy_(torch.randn(tuple(v.q.shape), generator=gen).to(torch.bfloat16).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    ref = pkv.pkv_decode_append(v.q, v.k_new, v.v_new, v.k_cache, v.v_cache, bt, ctx, int(wl.kv_lens.max()),
+                                wl.softmax_scale)
+    assert np.array_equal(bits(out), bits(ref))
+    expect_no_device_error(pkv)
