@@ -118,28 +118,22 @@ __device__ __forceinline__ void load_q(const Params& p, int b, int g, int r, flo
     }
 }
 
+// 16 dims of q . k: even and odd dims in the two halves of packed fp32x2 FMAs
+// (each product rounded as a scalar fmaf would, summed in the same two chains).
 __device__ __forceinline__ float dot16(const float (&qh)[16], const uint4& a, const uint4& c) {
     float s0 = 0.f, s1 = 0.f;
-    s0 = fmaf(qh[0], bf16_lo(a.x), s0);  s1 = fmaf(qh[1], bf16_hi(a.x), s1);
-    s0 = fmaf(qh[2], bf16_lo(a.y), s0);  s1 = fmaf(qh[3], bf16_hi(a.y), s1);
-    s0 = fmaf(qh[4], bf16_lo(a.z), s0);  s1 = fmaf(qh[5], bf16_hi(a.z), s1);
-    s0 = fmaf(qh[6], bf16_lo(a.w), s0);  s1 = fmaf(qh[7], bf16_hi(a.w), s1);
-    s0 = fmaf(qh[8], bf16_lo(c.x), s0);  s1 = fmaf(qh[9], bf16_hi(c.x), s1);
-    s0 = fmaf(qh[10], bf16_lo(c.y), s0); s1 = fmaf(qh[11], bf16_hi(c.y), s1);
-    s0 = fmaf(qh[12], bf16_lo(c.z), s0); s1 = fmaf(qh[13], bf16_hi(c.z), s1);
-    s0 = fmaf(qh[14], bf16_lo(c.w), s0); s1 = fmaf(qh[15], bf16_hi(c.w), s1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ffma2(s0, s1, qh[2 * i], qh[2 * i + 1], bf16_lo(w[i]), bf16_hi(w[i]), s0, s1);
     return s0 + s1;
 }
 
+// o += p * v over 16 dims, two dims per packed fp32x2 FMA.
 __device__ __forceinline__ void axpy16(float (&oh)[16], float pw, const uint4& a, const uint4& c) {
-    oh[0] = fmaf(pw, bf16_lo(a.x), oh[0]);   oh[1] = fmaf(pw, bf16_hi(a.x), oh[1]);
-    oh[2] = fmaf(pw, bf16_lo(a.y), oh[2]);   oh[3] = fmaf(pw, bf16_hi(a.y), oh[3]);
-    oh[4] = fmaf(pw, bf16_lo(a.z), oh[4]);   oh[5] = fmaf(pw, bf16_hi(a.z), oh[5]);
-    oh[6] = fmaf(pw, bf16_lo(a.w), oh[6]);   oh[7] = fmaf(pw, bf16_hi(a.w), oh[7]);
-    oh[8] = fmaf(pw, bf16_lo(c.x), oh[8]);   oh[9] = fmaf(pw, bf16_hi(c.x), oh[9]);
-    oh[10] = fmaf(pw, bf16_lo(c.y), oh[10]); oh[11] = fmaf(pw, bf16_hi(c.y), oh[11]);
-    oh[12] = fmaf(pw, bf16_lo(c.z), oh[12]); oh[13] = fmaf(pw, bf16_hi(c.z), oh[13]);
-    oh[14] = fmaf(pw, bf16_lo(c.w), oh[14]); oh[15] = fmaf(pw, bf16_hi(c.w), oh[15]);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        ffma2(oh[2 * i], oh[2 * i + 1], pw, pw, bf16_lo(w[i]), bf16_hi(w[i]), oh[2 * i], oh[2 * i + 1]);
 }
 
 // Write one piece's partial state (m, l, o) for both heads of the group.
