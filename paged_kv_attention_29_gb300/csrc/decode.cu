@@ -377,10 +377,10 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
             const float m_new = fmaxf(m[h], cm);
-            alpha[h] = exp2f(m[h] - m_new);
+            alpha[h] = ex2_ftz(m[h] - m_new);
             moved |= (m_new != m[h]);
             m[h] = m_new;
-            pr[h] = exp2f(sv - m_new);
+            pr[h] = ex2_ftz(sv - m_new);
             l[h] = fmaf(l[h], alpha[h], pr[h]);
         }
         if (moved) {
