@@ -180,6 +180,9 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                      const Params p) {
     // let the combine grid launch now; it waits for this grid's completion before reading
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this grid may itself start while the kernel before it (typically the previous step's
+    // combine) finishes: nothing global is touched before that kernel is complete
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1 KiB-aligned base
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageRegion);
@@ -439,6 +442,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 // One warp per (sequence, query head): merge its pieces in warp order.
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the next step's split-K may queue up
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the split-K grid's pieces are complete
     const int lane = threadIdx.x & 31;
     const int idx = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -566,11 +570,23 @@ pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream) {
             return PKV_ERR_CUDA;
         configured_device = dev;
     }
-    if (p.k_new != nullptr)
-        decode_splitk_kernel<true><<<W / WARPS, THREADS, smem, stream>>>(tm_k, tm_v, p);
-    else
-        decode_splitk_kernel<false><<<W / WARPS, THREADS, smem, stream>>>(tm_k, tm_v, p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    // both launches are programmatic dependents of what precedes them in the stream; each kernel
+    // waits (griddepcontrol.wait) for its predecessor's completion before touching global memory
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(W / WARPS);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = p.k_new != nullptr ? cudaLaunchKernelEx(&cfg, decode_splitk_kernel<true>, tm_k, tm_v, p)
+                                                 : cudaLaunchKernelEx(&cfg, decode_splitk_kernel<false>, tm_k, tm_v, p);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+    }
     // the combine is launched as a programmatic dependent of the split-K grid: its CTAs are
     // resident (waiting in griddepcontrol.wait) by the time the last split-K warp finishes
     const int n_rows = a.batch * a.num_heads;
@@ -579,9 +595,6 @@ pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream) {
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, decode_combine_kernel, p, a.num_heads, a.out) != cudaSuccess) return PKV_ERR_CUDA;
