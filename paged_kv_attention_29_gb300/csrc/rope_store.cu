@@ -105,6 +105,129 @@ __global__ void __launch_bounds__(kMaxThreads) rope_store_kernel(RopeStoreArgs a
     }
 }
 
+// ---------------------------------------------------------------------------
+// Staged path (head_dim 128, a token's rows within kMaxStageBytes): persistent
+// CTAs, two per SM, walk tokens t = blockIdx.x, + gridDim.x, ...  Per token a
+// stage of shared memory holds its Q, K and V rows:
+//   warp 0, lane 0   bulk-copies the three rows in (one mbarrier, "full");
+//   warps 1-4        rotate Q and K in place, thread (row r, word j) turning
+//                    the pairs (2j, 2j+64) and (2j+1, 2j+65) of rows r, r+4,
+//                    ... with its own two (cos, sin) -- no table, no CTA
+//                    barrier -- then arrive on "rotated";
+//   warp 5, lane 0   bulk-stores rotated Q to q_out, rotated K and the
+//                    untouched V straight from the stage to the pool slot,
+//                    and frees the stage ("empty") once its stores have read it.
+// kStages stages per CTA keep ~24 tokens per SM in flight.
+// ---------------------------------------------------------------------------
+constexpr int kStages = 12;
+constexpr int kStoresInFlight = 3;      // store groups still reading their stage
+constexpr int kRotWarps = 4;
+constexpr int kStagedThreads = 32 * (kRotWarps + 2);
+constexpr int kMaxStageBytes = 16384;
+
+__global__ void __launch_bounds__(kStagedThreads) rope_store_staged_kernel(RopeStoreArgs a, int64_t n_tokens,
+                                                                           int* err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int qb = a.q ? a.num_heads * 256 : 0;          // bytes of the Q rows (d = 128)
+    const int kvb = static_cast<int>(a.kv_row) * 2;
+    const int stage_bytes = qb + 2 * kvb;
+    const uint32_t stage0 = smem_u32(smem);
+    const uint32_t bars = stage0 + kStages * stage_bytes;   // full[S], rotated[S], empty[S]
+    auto full = [&](int s) { return bars + 8u * s; };
+    auto rotated = [&](int s) { return bars + 8u * (kStages + s); };
+    auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(rotated(s), 32 * kRotWarps);
+            mbar_init(empty(s), 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int64_t first = blockIdx.x;
+    const int64_t n_mine = first < n_tokens ? (n_tokens - first + gridDim.x - 1) / gridDim.x : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int64_t i = 0;
+            for (; i < n_mine; ++i) {
+                const int s = static_cast<int>(i % kStages);
+                if (i >= kStages && !mbar_wait(empty(s), static_cast<uint32_t>((i / kStages - 1) & 1), err, 1)) break;
+                const int64_t t = first + i * gridDim.x;
+                const uint32_t dst = stage0 + s * stage_bytes;
+                mbar_arrive_expect_tx(full(s), stage_bytes);
+                if (qb) bulk_load(dst, a.q + t * a.q_stride, qb, full(s));
+                bulk_load(dst + qb, a.k + t * a.k_stride, kvb, full(s));
+                bulk_load(dst + qb + kvb, a.v + t * a.v_stride, kvb, full(s));
+            }
+            // the last copies must land before the CTA's shared memory goes away (they have by the
+            // time the other roles are done; this matters only when a wait above gave up)
+            for (int64_t k = i > kStages ? i - kStages : 0; k < i; ++k)
+                mbar_wait(full(static_cast<int>(k % kStages)), static_cast<uint32_t>((k / kStages) & 1), err, 2);
+        }
+    } else if (warp <= kRotWarps) {
+        const int ct = threadIdx.x - 32;
+        const int j = ct & 31;                  // word j and j + 32 of a 128-element row
+        const int r0 = ct >> 5;                 // rows r0, r0 + 4, ...
+        const int hq = qb ? a.num_heads : 0;
+        const int rows = hq + a.num_kv_heads;
+        const uint64_t f0 = a.turns[2 * j], f1 = a.turns[2 * j + 1];
+        int pos_win = 0;                        // lane k: position of token i_base + k
+        for (int64_t i = 0; i < n_mine; ++i) {
+            if ((i & 31) == 0) {                // positions come 32 tokens at a time, off the per-token path
+                const int64_t ti = i + lane;
+                pos_win = ti < n_mine ? __ldg(a.positions + first + ti * gridDim.x) : 0;
+            }
+            const int s = static_cast<int>(i % kStages);
+            const bool ok = mbar_wait(full(s), static_cast<uint32_t>((i / kStages) & 1), err, 3);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const int pos = __shfl_sync(0xffffffffu, pos_win, static_cast<int>(i & 31));
+            float s0, c0, s1, c1;
+            __sincosf(reduced_angle(pos, static_cast<uint32_t>(f0), static_cast<uint32_t>(f0 >> 32)), &s0, &c0);
+            __sincosf(reduced_angle(pos, static_cast<uint32_t>(f1), static_cast<uint32_t>(f1 >> 32)), &s1, &c1);
+            uint32_t* st = reinterpret_cast<uint32_t*>(smem + s * stage_bytes);
+            for (int r = r0; r < rows; r += kRotWarps) {
+                uint32_t* w = st + (r < hq ? r * 64 : (qb >> 2) + (r - hq) * 64);
+                const uint32_t x1 = w[j], x2 = w[j + 32];
+                const float a0 = bf16_lo(x1), a1 = bf16_hi(x1), b0 = bf16_lo(x2), b1 = bf16_hi(x2);
+                w[j] = pack_bf16x2(fmaf(a0, c0, -b0 * s0), fmaf(a1, c1, -b1 * s1));
+                w[j + 32] = pack_bf16x2(fmaf(b0, c0, a0 * s0), fmaf(b1, c1, a1 * s1));
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the bulk stores
+            mbar_arrive(rotated(s));
+        }
+    } else {
+        // the whole warp walks the tokens (slots come 32 at a time, one per lane); lane 0 stores
+        int slot_win = -1;
+        for (int64_t i = 0; i < n_mine; ++i) {
+            if ((i & 31) == 0) {
+                const int64_t ti = i + lane;
+                slot_win = ti < n_mine ? __ldg(a.slots + first + ti * gridDim.x) : -1;
+            }
+            const int s = static_cast<int>(i % kStages);
+            const bool ok = mbar_wait(rotated(s), static_cast<uint32_t>((i / kStages) & 1), err, 4);
+            if (__any_sync(0xffffffffu, !ok)) break;
+            const int slot = __shfl_sync(0xffffffffu, slot_win, static_cast<int>(i & 31));
+            if (lane != 0) continue;
+            const int64_t t = first + i * gridDim.x;
+            const uint32_t src = stage0 + s * stage_bytes;
+            if (qb) bulk_store(a.q_out + t * a.q_out_stride, src, qb);
+            if (slot >= 0 && slot < a.num_slots) {
+                bulk_store(a.k_cache + static_cast<int64_t>(slot) * a.kv_row, src + qb, kvb);
+                bulk_store(a.v_cache + static_cast<int64_t>(slot) * a.kv_row, src + qb + kvb, kvb);
+            } else if (slot >= a.num_slots) {
+                record_error(err, PKV_DEVERR_SLOT, static_cast<int>(t));
+            }
+            bulk_commit();
+            bulk_wait_read<kStoresInFlight>();    // token i - kStoresInFlight's stores have read their stage
+            if (i >= kStoresInFlight) mbar_arrive(empty(static_cast<int>((i - kStoresInFlight) % kStages)));
+        }
+        if (lane == 0) bulk_wait<0>();           // all stores done before the shared memory is released
+    }
+}
+
 }  // namespace
 
 int rope_store_threads(const RopeStoreArgs& a) {
@@ -116,6 +239,23 @@ int rope_store_threads(const RopeStoreArgs& a) {
 
 cudaError_t launch_rope_store(const RopeStoreArgs& a, int64_t n_tokens, int* err, cudaStream_t stream) {
     if (n_tokens == 0) return cudaSuccess;
+    const int64_t stage = (a.q ? a.num_heads * 256 : 0) + 4 * a.kv_row;
+    if (a.head_dim == 128 && stage <= kMaxStageBytes) {
+        const size_t smem = static_cast<size_t>(kStages) * stage + 3 * kStages * 8;
+        static int configured_device = -1;
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (configured_device != dev) {
+            const cudaError_t e = cudaFuncSetAttribute(rope_store_staged_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kStages * kMaxStageBytes + 3 * kStages * 8));
+            if (e != cudaSuccess) return e;
+            configured_device = dev;
+        }
+        const int64_t grid = std::min<int64_t>(n_tokens, 2LL * sm_count());
+        rope_store_staged_kernel<<<static_cast<unsigned>(grid), kStagedThreads, smem, stream>>>(a, n_tokens, err);
+        return cudaGetLastError();
+    }
     const int threads = rope_store_threads(a);
     const int64_t grid = n_tokens;
     rope_store_kernel<<<static_cast<unsigned>(grid), threads, 0, stream>>>(a, n_tokens, err);
