@@ -299,15 +299,31 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) {
             int uq = 0, groups = 0;   // Q tiles and K/V groups issued
             // a tile's K or V: TMA from the physical block the table names (128 keys, two 64-dim halves)
-            auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t b, const Unit& w, int jj) {
+            // where tile jj of unit w lives: its physical block (from the block table) and the offset
+            // of its first key in that block
+            struct Loc {
+                int phys, off, g;
+            };
+            auto locate = [&](const Unit& w, int jj) {
                 const int key0 = jj * KT;
                 const int lb = key0 / p.block_size;
-                const int phys = __ldg(p.block_tables + static_cast<int64_t>(w.seq) * p.max_blocks + lb);
-                if (phys < 0 || phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, w.seq);
-                const int off = key0 - lb * p.block_size;
-                tma_load_4d(dst, map, b, 0, w.g, off, phys);
-                tma_load_4d(dst + HALF_BYTES, map, b, 64, w.g, off, phys);
+                Loc l;
+                l.phys = __ldg(p.block_tables + static_cast<int64_t>(w.seq) * p.max_blocks + lb);
+                if (l.phys < 0 || l.phys >= p.num_blocks) record_error(p.err, PKV_DEVERR_BLOCK_ID, w.seq);
+                l.off = key0 - lb * p.block_size;
+                l.g = w.g;
+                return l;
             };
+            auto load_tile = [&](const CUtensorMap* map, uint32_t dst, uint32_t b, const Loc& l) {
+                tma_load_4d(dst, map, b, 0, l.g, l.off, l.phys);
+                tma_load_4d(dst + HALF_BYTES, map, b, 64, l.g, l.off, l.phys);
+            };
+            // A group's V tile is the tile whose K went into the group before, so its block is known;
+            // the K tile's block is looked up one group early, after the previous group's copies are
+            // issued, so no block-table load sits between a stage's release and its refill.
+            Loc k_at = {0, 0, 0};                     // the tile of the last K copy
+            Loc pref = {0, 0, 0};
+            int pref_idx = -2, pref_tile = -1;        // what `pref` locates
             // one unit of lookahead: the next unit is taken when the current one starts (its first K
             // tile rides in the current unit's last group), so no CTA holds more than one unit it
             // has not started
@@ -315,8 +331,9 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             uint4 rec_cur = unit_record(p, idx_cur);
             bool ok = true;
             if (idx_cur >= 0) {                       // group 0: the first unit's first K tile
+                k_at = locate(unit_from(p, idx_cur, rec_cur), 0);
                 mbar_arrive_expect_tx(bar(BAR_GF), TILE_BYTES);
-                load_tile(&tm_k, sK, bar(BAR_GF), unit_from(p, idx_cur, rec_cur), 0);
+                load_tile(&tm_k, sK, bar(BAR_GF), k_at);
                 groups = 1;
             }
             int t = 0;                                // tiles of the units before the current one
@@ -329,6 +346,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (idx_cur < 0) break;
                 const int idx_nxt = grab_unit(p, total_units);  // its record is read for the last group
                 uint4 rec_nxt = make_uint4(0u, 0u, 0u, 0u);
+                bool rec_nxt_loaded = false;
                 const Unit u = unit_from(p, idx_cur, rec_cur);
                 const int n = max(u.n[0], u.n[1]);
                 if (uq >= 1 && !(ok = wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1))) break;
@@ -349,12 +367,30 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (gu >= 2 && !(ok = wait_phase(ctl, bar(BAR_GE + sg), ((gu - 2) >> 1) & 1))) break;
                     const bool k_here = j + 1 < n;
                     const bool k_next = !k_here && idx_nxt >= 0;
-                    if (k_next) rec_nxt = unit_record(p, idx_nxt);
+                    const Loc v_at = k_at;
+                    if (k_here) {
+                        k_at = (pref_idx == idx_cur && pref_tile == j + 1) ? pref : locate(u, j + 1);
+                    } else if (k_next) {
+                        if (!rec_nxt_loaded) rec_nxt = unit_record(p, idx_nxt);
+                        rec_nxt_loaded = true;
+                        k_at = (pref_idx == idx_nxt && pref_tile == 0) ? pref : locate(unit_from(p, idx_nxt, rec_nxt), 0);
+                    }
                     mbar_arrive_expect_tx(bar(BAR_GF + sg), (k_here || k_next) ? 2 * TILE_BYTES : TILE_BYTES);
-                    load_tile(&tm_v, sV + (sg ^ 1) * TILE_BYTES, bar(BAR_GF + sg), u, j);
-                    if (k_here) load_tile(&tm_k, sK + sg * TILE_BYTES, bar(BAR_GF + sg), u, j + 1);
-                    else if (k_next) load_tile(&tm_k, sK + sg * TILE_BYTES, bar(BAR_GF + sg), unit_from(p, idx_nxt, rec_nxt), 0);
+                    load_tile(&tm_v, sV + (sg ^ 1) * TILE_BYTES, bar(BAR_GF + sg), v_at);
+                    if (k_here || k_next) load_tile(&tm_k, sK + sg * TILE_BYTES, bar(BAR_GF + sg), k_at);
                     ++groups;
+                    // look up the next group's K tile now, while that group's stages are still in use
+                    if (j + 2 < n) {
+                        pref = locate(u, j + 2);
+                        pref_idx = idx_cur;
+                        pref_tile = j + 2;
+                    } else if (j + 2 == n && idx_nxt >= 0) {
+                        rec_nxt = unit_record(p, idx_nxt);
+                        rec_nxt_loaded = true;
+                        pref = locate(unit_from(p, idx_nxt, rec_nxt), 0);
+                        pref_idx = idx_nxt;
+                        pref_tile = 0;
+                    }
                 }
                 if (!ok) break;
                 t += n;
