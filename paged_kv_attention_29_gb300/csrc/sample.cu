@@ -114,18 +114,26 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
         // winner: some element of the warp already has a larger key.
         const int iters = (q1 - q0 + THREADS - 1) / THREADS;     // uniform across the CTA
         float wbest = -INFINITY;
+        // the next quad's logits are loaded one iteration ahead, so the load is in flight while
+        // this quad is examined
+        auto load_quad = [&](int qd, float (&l)[4]) {
+            const int col = qd * 4;
+            if (qd < q1 && vec_ok && col + 3 < vocab) {
+                const float4 l4 = __ldcs(reinterpret_cast<const float4*>(lrow + col));
+                l[0] = l4.x; l[1] = l4.y; l[2] = l4.z; l[3] = l4.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) l[e] = (qd < q1 && col + e < vocab) ? __ldcs(lrow + col + e) : -INFINITY;
+            }
+        };
+        float ln[4];
+        load_quad(q0 + tid, ln);
         for (int it = 0; it < iters; ++it) {
             const int qd = q0 + it * THREADS + tid;
+            float l[4] = {ln[0], ln[1], ln[2], ln[3]};
+            if (it + 1 < iters) load_quad(qd + THREADS, ln);
             if (qd < q1) {
                 const int col = qd * 4;
-                float l[4];
-                if (vec_ok && col + 3 < vocab) {
-                    const float4 l4 = __ldcs(reinterpret_cast<const float4*>(lrow + col));
-                    l[0] = l4.x; l[1] = l4.y; l[2] = l4.z; l[3] = l4.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) l[e] = (col + e < vocab) ? __ldcs(lrow + col + e) : -INFINITY;
-                }
                 const float best = fmaxf(bk, wbest);
                 const float lmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
                 // (NaN logits fail this test and go through the exact path, which rejects them)
