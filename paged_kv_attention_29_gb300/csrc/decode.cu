@@ -196,6 +196,14 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const int hkv = p.num_kv_heads;
     const int cap = p.max_blocks * p.block_size;
 
+    // the block tables are read right after the prefix below: have them on their way to L2 now
+    if (tid == 0) {
+        uint64_t bt_bytes = static_cast<uint64_t>(p.batch) * p.max_blocks * 4;
+        bt_bytes = (bt_bytes > (256u << 10) ? (256u << 10) : bt_bytes) & ~15ull;
+        if ((reinterpret_cast<uintptr_t>(p.block_tables) & 15) == 0 && bt_bytes > 0)
+            bulk_prefetch_l2(p.block_tables, static_cast<uint32_t>(bt_bytes));
+    }
+
     // ---- chunk counts per sequence and their prefix (every CTA computes the same)
     const int per = (p.batch + THREADS - 1) / THREADS;
     const int b0 = tid * per;
@@ -208,13 +216,21 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         }
         local += (L + CHUNK - 1) / CHUNK;
     }
-    tsum[tid] = local;
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int t = 0; t < THREADS; ++t) { const int x = tsum[t]; tsum[t] = run; run += x; }
-        prefix[p.batch] = run;
+    // exclusive scan of the per-thread counts: within each warp by shuffles, then over the warps
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
     }
+    if (lane == 31) tsum[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += tsum[w];
+    const int excl = before + incl - local;
+    __syncthreads();                        // every warp has read the warp totals
+    tsum[tid] = excl;
+    if (tid == THREADS - 1) prefix[p.batch] = excl + local;
     __syncthreads();
     {
         int run = tsum[tid];
@@ -452,7 +468,9 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
     const int g = h / G;
     const int hh = h - g * G;
     const int hkv = p.num_kv_heads;
-    const int n = p.plan[b + 1] - p.plan[b];
+    // the three plan entries in one round trip
+    const int plan_b = p.plan[b], plan_b1 = p.plan[b + 1], plan_all = p.plan[p.batch];
+    const int n = plan_b1 - plan_b;
     uint16_t* dst = out + static_cast<int64_t>(idx) * D + 4 * lane;
     if (n == 0) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
@@ -460,8 +478,8 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
         return;
     }
     const int64_t W = p.total_warps;
-    const int64_t total = static_cast<int64_t>(hkv) * p.plan[p.batch];
-    const int64_t start = static_cast<int64_t>(hkv) * p.plan[b] + static_cast<int64_t>(g) * n;
+    const int64_t total = static_cast<int64_t>(hkv) * plan_all;
+    const int64_t start = static_cast<int64_t>(hkv) * plan_b + static_cast<int64_t>(g) * n;
     const int64_t last = start + n - 1;
     const int wf = static_cast<int>(((start + 1) * W - 1) / total);
     const int wl = static_cast<int>(((last + 1) * W - 1) / total);
@@ -471,21 +489,56 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
     auto owns_chunks = [&](int w) {
         return (static_cast<int64_t>(w + 1) * total) / W > (static_cast<int64_t>(w) * total) / W;
     };
+    // pieces are read four at a time, every load of a batch issued before any is used
+    constexpr int BATCH = 4;
+    float mj[BATCH], lj[BATCH];
+    float4 vj[BATCH];
+    bool own[BATCH];
+    auto load_batch = [&](int w0) {
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            const int w = w0 + j;
+            own[j] = w <= wl && owns_chunks(w);
+            mj[j] = -INFINITY;
+            lj[j] = 0.f;
+            vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (own[j]) {
+                const int64_t slot = static_cast<int64_t>(q + w) * G + hh;
+                mj[j] = p.part_ml[slot * 2];
+                lj[j] = p.part_ml[slot * 2 + 1];
+                vj[j] = *reinterpret_cast<const float4*>(p.part_o + slot * D + 4 * lane);
+            }
+        }
+    };
+    const bool one_batch = wl - wf < BATCH;
     float M = -INFINITY;
-    for (int w = wf; w <= wl; ++w)
-        if (owns_chunks(w)) M = fmaxf(M, p.part_ml[(static_cast<int64_t>(q + w) * G + hh) * 2]);
+    if (one_batch) {
+        load_batch(wf);   // the usual case: every load of the merge in one round trip
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) M = fmaxf(M, mj[j]);
+    } else {
+        for (int w0 = wf; w0 <= wl; w0 += 32) {
+            const int w = w0 + lane;
+            if (w <= wl && owns_chunks(w)) M = fmaxf(M, p.part_ml[(static_cast<int64_t>(q + w) * G + hh) * 2]);
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    }
+    // merge in warp order
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = wf; w <= wl; ++w) {
-        if (!owns_chunks(w)) continue;
-        const int64_t slot = static_cast<int64_t>(q + w) * G + hh;
-        const float sc = exp2f(p.part_ml[slot * 2] - M);
-        L = fmaf(sc, p.part_ml[slot * 2 + 1], L);
-        const float4 v = *reinterpret_cast<const float4*>(p.part_o + slot * D + 4 * lane);
-        acc.x = fmaf(sc, v.x, acc.x);
-        acc.y = fmaf(sc, v.y, acc.y);
-        acc.z = fmaf(sc, v.z, acc.z);
-        acc.w = fmaf(sc, v.w, acc.w);
+    for (int w0 = wf; w0 <= wl; w0 += BATCH) {
+        if (!one_batch) load_batch(w0);
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            if (!own[j]) continue;
+            const float sc = exp2f(mj[j] - M);
+            L = fmaf(sc, lj[j], L);
+            acc.x = fmaf(sc, vj[j].x, acc.x);
+            acc.y = fmaf(sc, vj[j].y, acc.y);
+            acc.z = fmaf(sc, vj[j].z, acc.z);
+            acc.w = fmaf(sc, vj[j].w, acc.w);
+        }
     }
     const float inv = 1.f / L;
     uint2 packed;
