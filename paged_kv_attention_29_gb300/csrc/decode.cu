@@ -70,6 +70,14 @@ struct Params {
 
 __device__ __forceinline__ int seq_chunks(const int32_t* prefix, int b) { return prefix[b + 1] - prefix[b]; }
 
+// floor(a * b / c) for non-negative operands; `narrow` (a * b known to fit in 32 bits) takes
+// the unsigned 32-bit divide instead of the much longer 64-bit one.
+__device__ __forceinline__ int64_t mul_div(int64_t a, int64_t b, int64_t c, bool narrow) {
+    if (narrow)
+        return static_cast<int64_t>(static_cast<uint32_t>(a) * static_cast<uint32_t>(b) / static_cast<uint32_t>(c));
+    return a * b / c;
+}
+
 // Largest b with hkv * prefix[b] <= i  (prefix non-decreasing, prefix[0] = 0).
 __device__ __forceinline__ int locate_seq(const int32_t* prefix, int batch, int hkv, int64_t i) {
     int lo = 0, hi = batch;      // invariant: hkv*prefix[lo] <= i < hkv*prefix[hi]
@@ -89,7 +97,8 @@ __device__ __forceinline__ Cursor cursor_at(const int32_t* prefix, int batch, in
     cu.b = locate_seq(prefix, batch, hkv, i);
     cu.n = seq_chunks(prefix, cu.b);
     const int64_t rem = i - static_cast<int64_t>(hkv) * prefix[cu.b];
-    cu.g = static_cast<int>(rem / cu.n);
+    cu.g = rem <= 0xffffffffll ? static_cast<int>(static_cast<uint32_t>(rem) / static_cast<uint32_t>(cu.n))
+                               : static_cast<int>(rem / cu.n);
     cu.c = static_cast<int>(rem - static_cast<int64_t>(cu.g) * cu.n);
     return cu;
 }
@@ -250,8 +259,9 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     const int W = p.total_warps;
     const int gw = blockIdx.x * WARPS + warp;
     const int64_t total = static_cast<int64_t>(hkv) * prefix[p.batch];
-    const int64_t begin = static_cast<int64_t>(gw) * total / W;
-    const int64_t end = static_cast<int64_t>(gw + 1) * total / W;
+    const bool narrow = total * W <= 0xffffffffll;
+    const int64_t begin = mul_div(gw, total, W, narrow);
+    const int64_t end = mul_div(gw + 1, total, W, narrow);
     if (begin >= end) return;
     const int n_mine = static_cast<int>(end - begin);
 
@@ -481,13 +491,21 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
     const int64_t total = static_cast<int64_t>(hkv) * plan_all;
     const int64_t start = static_cast<int64_t>(hkv) * plan_b + static_cast<int64_t>(g) * n;
     const int64_t last = start + n - 1;
-    const int wf = static_cast<int>(((start + 1) * W - 1) / total);
-    const int wl = static_cast<int>(((last + 1) * W - 1) / total);
+    const bool narrow = total * W <= 0xffffffffll;
+    // the warp whose run holds chunk i: floor(((i + 1) W - 1) / total)
+    auto warp_of = [&](int64_t i) -> int {
+        if (narrow)
+            return static_cast<int>((static_cast<uint32_t>(i + 1) * static_cast<uint32_t>(W) - 1u) /
+                                    static_cast<uint32_t>(total));
+        return static_cast<int>(((i + 1) * W - 1) / total);
+    };
+    const int wf = warp_of(start);
+    const int wl = warp_of(last);
     const int q = b * hkv + g;
     // when the grid has more warps than chunks, some warps between wf and wl own
     // nothing and left no piece: skip them
     auto owns_chunks = [&](int w) {
-        return (static_cast<int64_t>(w + 1) * total) / W > (static_cast<int64_t>(w) * total) / W;
+        return mul_div(w + 1, total, W, narrow) > mul_div(w, total, W, narrow);
     };
     // pieces are read four at a time, every load of a batch issued before any is used
     constexpr int BATCH = 4;
@@ -495,27 +513,28 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
     float4 vj[BATCH];
     bool own[BATCH];
     auto load_batch = [&](int w0) {
+        // every slot q + w with w <= wl exists (q + wl < batch * Hkv + W), so the loads are
+        // issued first and a warp that owns no chunk (its slot is stale) is masked afterwards
 #pragma unroll
         for (int j = 0; j < BATCH; ++j) {
             const int w = w0 + j;
-            own[j] = w <= wl && owns_chunks(w);
-            mj[j] = -INFINITY;
-            lj[j] = 0.f;
-            vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (own[j]) {
+            if (w <= wl) {
                 const int64_t slot = static_cast<int64_t>(q + w) * G + hh;
                 mj[j] = p.part_ml[slot * 2];
                 lj[j] = p.part_ml[slot * 2 + 1];
                 vj[j] = *reinterpret_cast<const float4*>(p.part_o + slot * D + 4 * lane);
             }
         }
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) own[j] = w0 + j <= wl && owns_chunks(w0 + j);
     };
     const bool one_batch = wl - wf < BATCH;
     float M = -INFINITY;
     if (one_batch) {
         load_batch(wf);   // the usual case: every load of the merge in one round trip
 #pragma unroll
-        for (int j = 0; j < BATCH; ++j) M = fmaxf(M, mj[j]);
+        for (int j = 0; j < BATCH; ++j)
+            if (own[j]) M = fmaxf(M, mj[j]);
     } else {
         for (int w0 = wf; w0 <= wl; w0 += 32) {
             const int w = w0 + lane;
