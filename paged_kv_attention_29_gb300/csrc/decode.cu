@@ -24,6 +24,11 @@
 //   lanes by a transposing butterfly (14 shuffles for 16 values), leaving one
 //   token's score per lane; the chunk max is a warp max; the online-softmax
 //   rescale of o happens once per chunk and only when the max moved.
+// * Segment switches.  When a warp's run continues into the next (sequence,
+//   KV head), that segment's two query rows, new K/V row and length are copied
+//   into the warp's shared area by cp.async as soon as the current segment
+//   starts, so the switch reads shared memory instead of waiting on global
+//   loads while the warp's TMA stages sit idle.
 // * Combine.  A second kernel merges each (sequence, head)'s pieces in warp
 //   order with the log-sum-exp rule, so the result does not depend on timing.
 #include "pkv_device.cuh"
@@ -43,6 +48,9 @@ constexpr int MAX_BATCH = 4096;
 constexpr int THREADS = WARPS * 32;
 
 constexpr size_t kStageRegion = static_cast<size_t>(WARPS) * STAGES * STAGE_BYTES;
+// per warp: the next segment's G query rows, its new K and V rows, and its length
+constexpr int NEXT_BYTES = G * D * 2 + 2 * D * 2 + 16;
+constexpr size_t kNextRegion = static_cast<size_t>(WARPS) * NEXT_BYTES;
 
 struct Params {
     const uint16_t* q;
@@ -194,8 +202,8 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1 KiB-aligned base
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageRegion);
-    int32_t* prefix = reinterpret_cast<int32_t*>(smem + kStageRegion + WARPS * STAGES * 8);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStageRegion + kNextRegion);
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + kStageRegion + kNextRegion + WARPS * STAGES * 8);
     int32_t* tsum = prefix + (p.batch + 1);
     int32_t* stage_phys = tsum + THREADS;      // [WARPS][STAGES]: physical block of each staged chunk
 
@@ -331,6 +339,27 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         kv_row = __ldg(reinterpret_cast<const uint4*>((lane < 16 ? p.k_new : p.v_new) + src * D + (lane & 15) * 8));
     };
     load_new_row();
+    // the next segment's inputs, copied into this warp's shared area while this segment streams
+    const uint32_t next_base = smem_u32(smem + kStageRegion + static_cast<size_t>(warp) * NEXT_BYTES);
+    auto prefetch_next = [&](int k_at) {
+        if (n_mine - k_at <= cc.n - cc.c) return;   // the run ends inside this segment
+        Cursor nx = cc;
+        nx.c = nx.n - 1;
+        cursor_next(nx, prefix, p.batch, hkv);
+        const uint16_t* qrows = p.q + (static_cast<int64_t>(nx.b) * (hkv * G) + nx.g * G) * D;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(next_base + 16 * lane),
+                     "l"(qrows + 8 * lane) : "memory");
+        if (kFused) {
+            const int64_t src = static_cast<int64_t>(nx.b) * hkv + nx.g;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(next_base + G * D * 2 + 16 * lane),
+                         "l"((lane < 16 ? p.k_new : p.v_new) + src * D + (lane & 15) * 8) : "memory");
+        }
+        if (lane == 0)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(next_base + G * D * 2 + 2 * D * 2),
+                         "l"(p.context_lens + nx.b) : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    prefetch_next(0);
     bool failed = false;
     int consumed = 0;
 
@@ -441,9 +470,27 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             flush_piece(p, cc.b * hkv + cc.g + gw, lane, m, l, o);
             if (k != n_mine - 1) {
                 cursor_next(cc, prefix, p.batch, hkv);
-                load_q(p, cc.b, cc.g, r, qf);
-                Lb = min(max(__ldg(p.context_lens + cc.b), 0), cap);
-                load_new_row();
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const uint4 a = ld_shared_v4(next_base + h * D * 2 + 16 * r);
+                    const uint4 c = ld_shared_v4(next_base + h * D * 2 + 128 + 16 * r);
+                    const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        qf[h][2 * e] = bf16_lo(w[e]) * p.scale_log2;
+                        qf[h][2 * e + 1] = bf16_hi(w[e]) * p.scale_log2;
+                    }
+                }
+                if (kFused) kv_row = ld_shared_v4(next_base + G * D * 2 + 16 * lane);
+                {
+                    int len;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(len) : "r"(next_base + G * D * 2 + 2 * D * 2));
+                    Lb = min(max(len, 0), cap);
+                }
+                __syncwarp();   // every lane has read the area before the next copy lands in it
+                prefetch_next(k + 1);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     m[h] = -INFINITY;
@@ -456,6 +503,7 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             ++cc.c;
         }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (failed) {
         // let this warp's copies in flight land before the CTA's shared memory goes away
         for (int k = consumed; k < issued; ++k) {
@@ -567,7 +615,7 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
 }
 
 size_t dynamic_smem_bytes(int batch) {
-    return kStageRegion + WARPS * STAGES * 8 + static_cast<size_t>(batch + 1) * 4 + THREADS * 4 + WARPS * STAGES * 4 +
+    return kStageRegion + kNextRegion + WARPS * STAGES * 8 + static_cast<size_t>(batch + 1) * 4 + THREADS * 4 + WARPS * STAGES * 4 +
            1024;
 }
 
