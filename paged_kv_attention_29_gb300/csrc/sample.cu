@@ -98,6 +98,7 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
     int bi = -1;
     if (t_ok) {
         const float inv_t = 1.0f / T;
+        const float inv_t_log2e = inv_t * 1.4426950408889634f;
         const uint64_t rr = static_cast<uint64_t>(row) + offset;
         const uint32_t c1 = static_cast<uint32_t>(rr);
         const uint32_t c2 = static_cast<uint32_t>(rr >> 32);
@@ -111,9 +112,12 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
         // 1 - u < e^-t.  And -ln(-ln u) <= 16.64 for every u the generator makes
         // (u <= 1 - 2^-24), so a quad whose largest l/T + 16.7 is below `best` has
         // no candidate at all and skips its Philox call.  `best` is the warp's
-        // running maximum; t carries a 1e-3 margin so rounding and exact ties are
-        // always decided by the exact key.  Skipped elements cannot change the
-        // winner: some element of the warp already has a larger key.
+        // running maximum; t carries a 1e-3 margin and the bound a factor 1.001,
+        // so rounding and exact ties are always decided by the exact key.  Within
+        // a quad that does draw noise, the per-element test has no branch; only a
+        // quad with a candidate branches to the exact key.  Skipped elements
+        // cannot change the winner: some element of the warp already has a
+        // larger key.
         const int iters = (q1 - q0 + THREADS - 1) / THREADS;     // uniform across the CTA
         float wbest = -INFINITY;
         // the next quad's logits are loaded one iteration ahead, so the load is in flight while
@@ -138,32 +142,33 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
                 const int col = qd * 4;
                 const float best = fmaxf(bk, wbest);
                 const float lmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
-                // (NaN logits fail this test and go through the exact path, which rejects them)
+                // (NaN logits fail this test; their bound below is NaN, so they are never candidates)
                 if (!(lmax * inv_t + 16.7f < best)) {
                     const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(qd), c1, c2, 0u), key0, key1);
                     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                    // candidate test, branch-free: 1 - u < 1.001 e^-t, t = best - l/T - 1e-3, as
+                    // 1 - u < 2^(l (log2 e / T) + cb).  t <= 0 gives a bound above 1 (always a
+                    // candidate); l = -inf (padding past the vocabulary) gives 0 (never); NaN never.
+                    const float cb = (1e-3f - best) * 1.4426950408889634f + 1.4419741739064e-3f;   // + log2 1.001
+                    bool cand[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        if (col + e >= vocab) continue;
-                        const float t = best - l[e] * inv_t - 1e-3f;
-                        if (t > 0.f) {
-                            // 1 - u exactly: (2^24 - (2 (x >> 9) + 1)) 2^-24
-                            const float one_minus_u =
-                                __uint2float_rn(16777216u - (2u * (xs[e] >> 9) + 1u)) * 5.9604644775390625e-08f;
-                            // ex2.approx is within 2^-22 relatively, well inside the 1.001 margin; a
-                            // bound flushed to zero only skips elements that cannot win (1 - u >= 2^-24)
-                            const float bound = ex2_ftz(-t * 1.4426950408889634f) * 1.001f;
-                            if (one_minus_u >= bound) continue;
-                        }
-                        consider(l[e], inv_t, xs[e], col + e, bk, bi);
+                        // 1 - u exactly: f = 1 + (x >> 9) 2^-23 in [1, 2), 1 - u = (2 - f) - 2^-24
+                        const float f = __uint_as_float(0x3F800000u | (xs[e] >> 9));
+                        const float one_minus_u = (2.0f - f) - 5.9604644775390625e-08f;
+                        // ex2.approx is within 2^-22 relatively, well inside the 1.001 margin; a
+                        // bound flushed to zero only skips elements that cannot win (1 - u >= 2^-24)
+                        cand[e] = one_minus_u < ex2_ftz(fmaf(l[e], inv_t_log2e, cb));
+                    }
+                    if (cand[0] | cand[1] | cand[2] | cand[3]) {   // rare once `best` has settled
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (cand[e]) consider(l[e], inv_t, xs[e], col + e, bk, bi);
                     }
                 }
             }
-            // share the running best across the warp
-            float m = bk;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            wbest = m;
+            // share the running best across the warp (NaN never enters a key)
+            asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wbest) : "f"(bk));
         }
     } else if (rank == 0 && tid == 0) {
         record_error(err, PKV_DEVERR_TEMPERATURE, row);

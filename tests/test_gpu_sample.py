@@ -86,3 +86,29 @@ def test_sample_frequencies_follow_softmax(pkv):
     ids = pkv.pkv_sample(logits, torch.full((n,), T).cuda(), seed=99)
     freq = np.bincount(ids.cpu().numpy(), minlength=4) / n
     assert np.all(np.abs(freq - p) < 4 * np.sqrt(p * (1 - p) / n)), freq
+
+
+def test_sample_masked_and_nan_logits(pkv):
+    """-inf logits (a masked vocabulary) never win and NaN logits never win; a row with a
+    single finite logit returns it, a row with none returns -1.  The other rows match the
+    oracle run on the same logits with NaN replaced by -inf."""
+    s = W.sampler_inputs(batch=64, vocab=5000, seed=34, device="cpu")
+    lg = s.logits.clone()
+    g = torch.Generator().manual_seed(35)
+    lg[torch.rand(lg.shape, generator=g) < 0.9] = -float("inf")
+    lg[0, :] = -float("inf")
+    lg[0, 17] = 2.0
+    lg[1, :] = -float("inf")
+    nan_at = torch.rand(lg.shape, generator=g) < 0.01
+    nan_at[0, 17] = False
+    lg[nan_at] = float("nan")
+    ids = pkv.pkv_sample(lg.cuda(), s.temperatures.cuda(), s.seed, s.offset).cpu().numpy()
+    assert ids[0] == 17 and ids[1] == -1
+    rows = np.array([b for b in range(64) if b != 1])
+    ref_in = lg.double().numpy()
+    ref_in[np.isnan(ref_in)] = -np.inf
+    e = sm.exponential_noise(s.seed, s.offset, range(64), lg.shape[1])
+    ref, margin = sm.exponential_race(ref_in[rows], s.temperatures.double().numpy()[rows], e[rows])
+    clear = margin >= NEAR_TIE
+    assert np.array_equal(ids[rows][clear], ref[clear])
+    assert np.all(np.isfinite(ref_in[rows, ids[rows]]))
