@@ -35,18 +35,41 @@ constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
 constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
 constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Philox4x32-10 (ten rounds of two 32x32 -> 64 products, the high halves xored into the
+// other words with the round key, which advances by the Weyl increments) for the counters
+// (q, c1, c2, 0) of one row: the words that do not depend on q make round 0's second
+// product and round 1's first product row constants, computed once.
+struct PhiloxRow {
+    uint32_t x0, y0, p_hi, p_lo, k0, k1;
+};
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t c1, uint32_t c2, uint32_t k0, uint32_t k1) {
+    PhiloxRow r;
+    const uint64_t a = static_cast<uint64_t>(kPhiloxM1) * c2;
+    r.x0 = static_cast<uint32_t>(a >> 32) ^ c1 ^ k0;
+    r.y0 = static_cast<uint32_t>(a);
+    const uint64_t p = static_cast<uint64_t>(kPhiloxM0) * r.x0;
+    r.p_hi = static_cast<uint32_t>(p >> 32);
+    r.p_lo = static_cast<uint32_t>(p);
+    r.k0 = k0;
+    r.k1 = k1;
+    return r;
+}
+__device__ __forceinline__ uint4 philox_row_at(uint32_t q, const PhiloxRow& r) {
+    uint32_t k0 = r.k0, k1 = r.k1;
+    const uint64_t b = static_cast<uint64_t>(kPhiloxM0) * q;            // round 0
+    const uint32_t z0 = static_cast<uint32_t>(b >> 32) ^ k1, w0 = static_cast<uint32_t>(b);
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+    const uint64_t d = static_cast<uint64_t>(kPhiloxM1) * z0;           // round 1
+    uint4 c = make_uint4(static_cast<uint32_t>(d >> 32) ^ r.y0 ^ k0, static_cast<uint32_t>(d), r.p_hi ^ w0 ^ k1, r.p_lo);
 #pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        if (round) {
-            k0 += kPhiloxW0;
-            k1 += kPhiloxW1;
-        }
-        const uint32_t lo0 = kPhiloxM0 * c.x;
-        const uint32_t hi0 = __umulhi(kPhiloxM0, c.x);
-        const uint32_t lo1 = kPhiloxM1 * c.z;
-        const uint32_t hi1 = __umulhi(kPhiloxM1, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    for (int round = 2; round < 10; ++round) {
+        k0 += kPhiloxW0;
+        k1 += kPhiloxW1;
+        const uint64_t e0 = static_cast<uint64_t>(kPhiloxM0) * c.x;
+        const uint64_t e1 = static_cast<uint64_t>(kPhiloxM1) * c.z;
+        c = make_uint4(static_cast<uint32_t>(e1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(e1),
+                       static_cast<uint32_t>(e0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(e0));
     }
     return c;
 }
@@ -102,6 +125,7 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
         const uint64_t rr = static_cast<uint64_t>(row) + offset;
         const uint32_t c1 = static_cast<uint32_t>(rr);
         const uint32_t c2 = static_cast<uint32_t>(rr >> 32);
+        const PhiloxRow prow = philox_row(c1, c2, key0, key1);
         const float* lrow = logits + static_cast<int64_t>(row) * row_stride;
         const int nquads = (vocab + 3) >> 2;
         const int per = (nquads + CLUSTER - 1) / CLUSTER;
@@ -144,7 +168,7 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
                 const float lmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
                 // (NaN logits fail this test; their bound below is NaN, so they are never candidates)
                 if (!(lmax * inv_t + 16.7f < best)) {
-                    const uint4 x = philox4x32_10(make_uint4(static_cast<uint32_t>(qd), c1, c2, 0u), key0, key1);
+                    const uint4 x = philox_row_at(static_cast<uint32_t>(qd), prow);
                     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
                     // candidate test, branch-free: 1 - u < 1.001 e^-t, t = best - l/T - 1e-3, as
                     // 1 - u < 2^(l (log2 e / T) + cb).  t <= 0 gives a bound above 1 (always a

@@ -112,3 +112,12 @@ def test_sample_masked_and_nan_logits(pkv):
     clear = margin >= NEAR_TIE
     assert np.array_equal(ids[rows][clear], ref[clear])
     assert np.all(np.isfinite(ref_in[rows, ids[rows]]))
+
+
+def test_sample_offset_across_the_32_bit_boundary(pkv):
+    """Counter word 2 is (row + offset) >> 32: an offset just below 2^32 puts the first rows at
+    c2 = 0 and the rest at c2 = 1, and a seed with both halves set drives both key words."""
+    s = W.sampler_inputs(batch=24, vocab=2051, seed=36, device="cpu")
+    seed, offset = 0x123456789ABCDEF0, 2 ** 32 - 3
+    ids = pkv.pkv_sample(s.logits.cuda(), s.temperatures.cuda(), seed, offset)
+    _check_ids(ids, s.logits, s.temperatures, seed, offset)
