@@ -729,14 +729,16 @@ def main(argv=None):
     secondary = {"unfused_decode_step": head["unfused"]}
     parts = set() if args.no_secondary else {x.strip() for x in args.parts.split(",") if x.strip()}
     if rank == 0:
-        if "prefill" in parts:
-            secondary["prefill"] = bench_prefill(args, pkv, torch, peaks)
-        if "long" in parts:
-            secondary["long_decode"] = bench_long_decode(args, pkv, torch, peaks)
-        if "full" in parts:
-            secondary["full_step"] = bench_full_step(args, pkv, torch, peaks)
-        if "rope" in parts:
-            secondary["rope_store"] = bench_rope_store(args, pkv, torch, peaks)
+        # each part runs inside an NVTX range of its own name, so a profiler can select one
+        # (ncu --nvtx --nvtx-include "full_step/")
+        for key, part, fn in (("prefill", "prefill", bench_prefill), ("long", "long_decode", bench_long_decode),
+                              ("full", "full_step", bench_full_step), ("rope", "rope_store", bench_rope_store)):
+            if key in parts:
+                torch.cuda.nvtx.range_push(part)
+                try:
+                    secondary[part] = fn(args, pkv, torch, peaks)
+                finally:
+                    torch.cuda.nvtx.range_pop()
     code, info = pkv.pkv_get_device_error(clear=True)
     if code:
         raise RuntimeError(f"device error {code} ({pkv.DEVERR.get(code)}), info {info}")
