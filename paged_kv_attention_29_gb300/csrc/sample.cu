@@ -54,18 +54,28 @@ __device__ __forceinline__ PhiloxRow philox_row(uint32_t c1, uint32_t c2, uint32
     r.k1 = k1;
     return r;
 }
-__device__ __forceinline__ uint4 philox_row_at(uint32_t q, const PhiloxRow& r) {
-    uint32_t k0 = r.k0, k1 = r.k1;
+// The ten round keys of both words.  With a host seed they are computed on the host and
+// read from the kernel's parameters, so the rounds spend no instruction on them.
+struct RoundKeys {
+    uint32_t k0[10], k1[10];
+};
+template <bool kParamKeys>
+__device__ __forceinline__ uint32_t round_key(const RoundKeys& rk, uint32_t base, int word, int round) {
+    if (kParamKeys) return word == 0 ? rk.k0[round] : rk.k1[round];
+    return base + static_cast<uint32_t>(round) * (word == 0 ? kPhiloxW0 : kPhiloxW1);
+}
+template <bool kParamKeys>
+__device__ __forceinline__ uint4 philox_row_at(uint32_t q, const PhiloxRow& r, const RoundKeys& rk) {
     const uint64_t b = static_cast<uint64_t>(kPhiloxM0) * q;            // round 0
-    const uint32_t z0 = static_cast<uint32_t>(b >> 32) ^ k1, w0 = static_cast<uint32_t>(b);
-    k0 += kPhiloxW0;
-    k1 += kPhiloxW1;
+    const uint32_t z0 = static_cast<uint32_t>(b >> 32) ^ round_key<kParamKeys>(rk, r.k1, 1, 0);
+    const uint32_t w0 = static_cast<uint32_t>(b);
     const uint64_t d = static_cast<uint64_t>(kPhiloxM1) * z0;           // round 1
-    uint4 c = make_uint4(static_cast<uint32_t>(d >> 32) ^ r.y0 ^ k0, static_cast<uint32_t>(d), r.p_hi ^ w0 ^ k1, r.p_lo);
+    uint4 c = make_uint4(static_cast<uint32_t>(d >> 32) ^ r.y0 ^ round_key<kParamKeys>(rk, r.k0, 0, 1),
+                         static_cast<uint32_t>(d), r.p_hi ^ w0 ^ round_key<kParamKeys>(rk, r.k1, 1, 1), r.p_lo);
 #pragma unroll
     for (int round = 2; round < 10; ++round) {
-        k0 += kPhiloxW0;
-        k1 += kPhiloxW1;
+        const uint32_t k0 = round_key<kParamKeys>(rk, r.k0, 0, round);
+        const uint32_t k1 = round_key<kParamKeys>(rk, r.k1, 1, round);
         const uint64_t e0 = static_cast<uint64_t>(kPhiloxM0) * c.x;
         const uint64_t e1 = static_cast<uint64_t>(kPhiloxM1) * c.z;
         c = make_uint4(static_cast<uint32_t>(e1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(e1),
@@ -94,11 +104,14 @@ __device__ __forceinline__ void consider(float logit, float inv_t, uint32_t x, i
     }
 }
 
+// kParamKeys: the seed came from the host and `rk` holds its round keys; otherwise the
+// seed and row offset are read from `seed_offset` and the keys computed here.
+template <bool kParamKeys>
 __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS)
 sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stride,
                    const float* __restrict__ temperatures, uint32_t key0, uint32_t key1,
                    uint64_t offset, const uint64_t* __restrict__ seed_offset, int vec_ok,
-                   int64_t* __restrict__ out_ids, int* err) {
+                   int64_t* __restrict__ out_ids, int* err, const RoundKeys rk) {
     __shared__ float s_key[THREADS / 32];
     __shared__ int s_idx[THREADS / 32];
     __shared__ float c_key;
@@ -109,7 +122,7 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
     const int row = blockIdx.y;
     const int tid = threadIdx.x;
     const float T = __ldg(temperatures + row);
-    if (seed_offset != nullptr) {          // seed and row offset from device memory
+    if (!kParamKeys) {                      // seed and row offset from device memory
         const uint64_t sd = __ldg(seed_offset);
         key0 = static_cast<uint32_t>(sd);
         key1 = static_cast<uint32_t>(sd >> 32);
@@ -168,7 +181,7 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
                 const float lmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
                 // (NaN logits fail this test; their bound below is NaN, so they are never candidates)
                 if (!(lmax * inv_t + 16.7f < best)) {
-                    const uint4 x = philox_row_at(static_cast<uint32_t>(qd), prow);
+                    const uint4 x = philox_row_at<kParamKeys>(static_cast<uint32_t>(qd), prow, rk);
                     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
                     // candidate test, branch-free: 1 - u < 1.001 e^-t, t = best - l/T - 1e-3, as
                     // 1 - u < 2^(l (log2 e / T) + cb).  t <= 0 gives a bound above 1 (always a
@@ -235,10 +248,19 @@ cudaError_t launch_sample(const float* logits, int batch, int vocab, int64_t row
     if (batch == 0) return cudaSuccess;
     const int vec_ok = ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) && (row_stride % 4 == 0);
     dim3 grid(CLUSTER, batch);
-    sample_race_kernel<<<grid, THREADS, 0, stream>>>(logits, vocab, row_stride, temperatures,
-                                                     static_cast<uint32_t>(seed),
-                                                     static_cast<uint32_t>(seed >> 32), offset, seed_offset,
-                                                     vec_ok, out_ids, err);
+    RoundKeys rk = {};
+    const uint32_t key0 = static_cast<uint32_t>(seed), key1 = static_cast<uint32_t>(seed >> 32);
+    if (seed_offset == nullptr) {
+        for (int r = 0; r < 10; ++r) {
+            rk.k0[r] = key0 + static_cast<uint32_t>(r) * kPhiloxW0;
+            rk.k1[r] = key1 + static_cast<uint32_t>(r) * kPhiloxW1;
+        }
+        sample_race_kernel<true><<<grid, THREADS, 0, stream>>>(logits, vocab, row_stride, temperatures, key0, key1,
+                                                               offset, nullptr, vec_ok, out_ids, err, rk);
+    } else {
+        sample_race_kernel<false><<<grid, THREADS, 0, stream>>>(logits, vocab, row_stride, temperatures, key0,
+                                                                key1, offset, seed_offset, vec_ok, out_ids, err, rk);
+    }
     return cudaGetLastError();
 }
 
