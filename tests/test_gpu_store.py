@@ -63,26 +63,37 @@ def test_store_kvcache_bit_exact(pkv, name):
     expect_no_device_error(pkv)
 
 
-def test_store_skips_padding_and_flags_out_of_pool(pkv):
-    nb, bs = 3, 256
-    k = torch.randn(3, 8, 128, device="cuda").to(torch.bfloat16)
-    v = torch.randn(3, 8, 128, device="cuda").to(torch.bfloat16)
+@pytest.mark.parametrize("n", [3, 2048])
+def test_store_skips_padding_and_flags_out_of_pool(pkv, n):
+    """Slot -1 (padding) is skipped and a slot past the pool is flagged; 2048 tokens take the
+    staged bulk-copy path, 3 the one-CTA-per-token path."""
+    nb, bs = 16, 256
+    g = torch.Generator().manual_seed(51)
+    k = torch.randn(n, 8, 128, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(n, 8, 128, generator=g).to(torch.bfloat16).cuda()
     kc = torch.zeros(nb, bs, 8, 128, dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
-    slots = torch.tensor([5, -1, nb * bs + 3], dtype=torch.int32, device="cuda")
-    pkv.pkv_store_kvcache(k, v, slots, kc, vc)
+    slots = torch.randperm(nb * bs, generator=g)[:n].to(torch.int32)
+    pad = torch.arange(n) % 7 == 1                 # every seventh token is padding
+    slots[pad] = -1
+    bad = n - 1 if n > 3 else 2                    # exactly one slot past the pool
+    slots[bad] = nb * bs + 3
+    pkv.pkv_store_kvcache(k, v, slots.cuda(), kc, vc)
     torch.cuda.synchronize()
-    assert torch.equal(kc[0, 5], k[0]) and torch.equal(vc[0, 5], v[0])
-    kc[0, 5] = 0
-    vc[0, 5] = 0
-    assert int(kc.count_nonzero()) == 0 and int(vc.count_nonzero()) == 0
+    ok = (slots >= 0) & (slots < nb * bs)
+    flat_k, flat_v = kc.view(nb * bs, 8, 128).cpu(), vc.view(nb * bs, 8, 128).cpu()
+    assert torch.equal(flat_k[slots[ok].long()], k.cpu()[ok]) and torch.equal(flat_v[slots[ok].long()], v.cpu()[ok])
+    untouched = torch.ones(nb * bs, dtype=torch.bool)
+    untouched[slots[ok].long()] = False
+    assert int(flat_k[untouched].count_nonzero()) == 0 and int(flat_v[untouched].count_nonzero()) == 0
     code, info = pkv.pkv_get_device_error(clear=True)
-    assert code == 2 and info == 2
+    assert code == 2 and info == bad
 
 
-def test_store_from_fused_qkv_rows(pkv):
+@pytest.mark.parametrize("n", [37, 3000])
+def test_store_from_fused_qkv_rows(pkv, n):
     """k and v may be strided views into one [n, (16+8+8)*128] projection output."""
-    n, nb, bs = 37, 4, 256
+    nb, bs = 16, 256
     qkv = torch.randn(n, (16 + 8 + 8) * 128, device="cuda").to(torch.bfloat16)
     k = qkv[:, 16 * 128:24 * 128].view(n, 8, 128)
     v = qkv[:, 24 * 128:].view(n, 8, 128)
