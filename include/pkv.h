@@ -214,6 +214,7 @@ PKV_API pkv_status pkv_prefill_varlen(const pkv_bf16 *q, const pkv_bf16 *k_cache
  *   workspace  >= pkv_decode_workspace_size(batch, num_heads, num_kv_heads,
  *        head_dim) bytes on the current device, 256-byte aligned; its contents
  *        need no initialisation and are scratch after the call
+ * batch <= 4096 (PKV_ERR_UNSUPPORTED above, before any launch).
  * The work is split over the GPU's warps into equal runs of KV; partial
  * softmax states are merged in a fixed order, so results are deterministic.
  */

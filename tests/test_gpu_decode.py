@@ -186,3 +186,30 @@ def test_prepared_decode_append_call(pkv):
     assert np.array_equal(bits(out), bits(o_ref2))
     assert not np.array_equal(bits(o_ref2), bits(o_ref))
     expect_no_device_error(pkv)
+
+
+def test_decode_at_the_batch_limit(pkv):
+    """4096 sequences, the largest batch (the chunk-prefix scan then sums 32 sequences per
+    thread), over a small pool that the sequences share read-only through random block tables;
+    zero-length rows come out zero; sampled rows against the oracle.  4097 is refused."""
+    B, nb, bs, hq, hkv, d = 4096, 64, 256, 16, 8, 128
+    g = torch.Generator().manual_seed(61)
+    kc = torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16)
+    vc = torch.randn(nb, bs, hkv, d, generator=g).to(torch.bfloat16)
+    q = torch.randn(B, hq, d, generator=g).to(torch.bfloat16)
+    lens = torch.randint(0, 2 * bs + 1, (B,), generator=g).to(torch.int32)
+    lens[::97] = 0
+    bt = torch.randint(0, nb, (B, 2), generator=g).to(torch.int32)
+    scale = d ** -0.5
+    out = pkv.pkv_decode(q.cuda(), kc.cuda(), vc.cuda(), bt.cuda(), lens.cuda(), 2 * bs, scale)
+    rows = list(range(0, B, 41)) + [B - 1]
+    ref = pa.decode_rows(f32(q), f32(kc), f32(vc), bt.numpy(), lens.numpy(), bs, scale, rows)
+    assert_attention_close(out[rows], ref, "batch 4096")
+    zero = torch.nonzero(lens == 0).flatten().tolist()
+    assert torch.count_nonzero(out[zero]).item() == 0
+    expect_no_device_error(pkv)
+    q2 = torch.zeros(B + 1, hq, d, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_decode(q2, kc.cuda(), vc.cuda(), torch.zeros(B + 1, 2, dtype=torch.int32, device="cuda"),
+                       torch.ones(B + 1, dtype=torch.int32, device="cuda"), 2 * bs, scale)
+    assert e.value.status == 2                        # PKV_ERR_UNSUPPORTED
