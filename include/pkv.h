@@ -325,6 +325,17 @@ PKV_API pkv_status pkv_sample_dev(const float *logits, int32_t batch, int32_t vo
  */
 PKV_API pkv_status pkv_get_device_error(int32_t *code, int32_t *info, int32_t clear);
 
+/*
+ * Failure-path check.  Launches one CTA that waits, through the same bounded
+ * mbarrier wait every kernel here uses, on a barrier that nothing completes.
+ * The wait gives up after its limit (2 s), records PKV_DEVERR_TIMEOUT with
+ * info PKV_WAIT_CHECK_INFO in the device error word, and the kernel returns:
+ * no trap and no fault, so the context stays usable.  Asynchronous on
+ * `stream`; read the result with pkv_get_device_error().
+ */
+#define PKV_WAIT_CHECK_INFO 0x5741
+PKV_API pkv_status pkv_check_wait_timeout(pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,8 @@ import torch
 __all__ = [
     "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
     "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
-    "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error",
+    "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error", "pkv_check_wait_timeout",
+    "WAIT_CHECK_INFO",
     "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "pkv_sample_dev", "pkv_rope_store_kvcache", "DecodeAppendCall", "DEVERR",
 ]
 
@@ -95,6 +96,7 @@ def load() -> ctypes.CDLL:
                                       _c_ptr]),
         "pkv_sample_dev": (ctypes.c_int, [_c_ptr, _c_int32, _c_int32, _c_int64, _c_ptr, _c_ptr, _c_ptr, _c_ptr]),
         "pkv_get_device_error": (ctypes.c_int, [ctypes.POINTER(_c_int32), ctypes.POINTER(_c_int32), _c_int32]),
+        "pkv_check_wait_timeout": (ctypes.c_int, [ctypes.c_void_p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -431,6 +433,15 @@ def pkv_sample_dev(logits: torch.Tensor, temperatures: torch.Tensor, seed_offset
     _raise(load().pkv_sample_dev(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures), _ptr(seed_offset),
                                  _ptr(out_ids), _stream(stream)), "pkv_sample_dev")
     return out_ids
+
+
+WAIT_CHECK_INFO = 0x5741
+
+
+def pkv_check_wait_timeout(stream=None) -> None:
+    """Run the failure-path check: one wait that nothing completes gives up after its limit
+    (about 2 s) and records (DEVERR timeout, WAIT_CHECK_INFO); read it with pkv_get_device_error."""
+    _raise(load().pkv_check_wait_timeout(_stream(stream)), "pkv_check_wait_timeout")
 
 
 def pkv_get_device_error(clear: bool = True):

@@ -6,6 +6,7 @@
 #include <math.h>
 #include <mutex>
 
+#include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -64,6 +65,19 @@ cudaStream_t as_stream(pkv_stream_t s) { return static_cast<cudaStream_t>(s); }
 bool supported_shape(int num_heads, int num_kv_heads, int head_dim, int block_size) {
     return head_dim == kHeadDim && num_kv_heads > 0 && num_heads == kGroup * num_kv_heads &&
            block_size > 0 && block_size % kBlockQuantum == 0;
+}
+
+// One thread waits on a barrier that nothing completes, through the bounded wait all the
+// kernels use; it gives up after the limit, records the timeout and the kernel returns.
+__global__ void wait_check_kernel(int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(b, 0, err, PKV_WAIT_CHECK_INFO);
 }
 
 }  // namespace
@@ -378,6 +392,13 @@ pkv_status pkv_sample_dev(const float* logits, int32_t batch, int32_t vocab, int
     const cudaError_t e = launch_sample(logits, batch, vocab, row_stride, temperatures, 0, 0, seed_offset, out_ids,
                                         err, as_stream(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_check_wait_timeout(pkv_stream_t stream) {
+    int* err = device_error_word();
+    if (!err) return PKV_ERR_CUDA;
+    wait_check_kernel<<<1, 32, 0, as_stream(stream)>>>(err);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status pkv_get_device_error(int32_t* code, int32_t* info, int32_t clear) {
