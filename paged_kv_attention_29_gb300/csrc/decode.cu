@@ -431,9 +431,8 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const float sv = valid ? sc[h] : -INFINITY;
-            float cm = sv;
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+            float cm;   // the chunk max over the warp in one reduction (no NaN reaches it: sv is a score or -inf)
+            asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(cm) : "f"(sv));
             const float m_new = fmaxf(m[h], cm);
             alpha[h] = ex2_ftz(m[h] - m_new);
             moved |= (m_new != m[h]);
