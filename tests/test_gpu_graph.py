@@ -1,14 +1,15 @@
-"""A decode step captured in a CUDA graph and replayed (atlas fig. 26: a replay
-reads new inputs from pre-allocated buffers; shapes and addresses are fixed,
-values may change).  The captured step -- two layers of pkv_decode_append and
+"""Steps captured in a CUDA graph and replayed (atlas fig. 26: a replay reads
+new inputs from pre-allocated buffers; shapes and addresses are fixed, values
+may change).  The captured decode step -- two layers of pkv_decode_append and
 pkv_sample_dev, whose noise offset lives in device memory and advances inside
-the graph -- must give, replay after replay, exactly what the eager calls give."""
+the graph -- and the captured prefill step (slot mapping, KV scatter, prefill)
+must give, replay after replay, exactly what the eager calls give."""
 import numpy as np
 import pytest
 import torch
 
 import workloads as W
-from pkv_testutil import bits, expect_no_device_error
+from pkv_testutil import GpuBatch, bits, expect_no_device_error
 
 pytestmark = pytest.mark.gpu
 
@@ -95,4 +96,46 @@ def test_prepared_call_made_before_capture_is_captured(pkv):
     ref = pkv.pkv_decode_append(v.q, v.k_new, v.v_new, v.k_cache, v.v_cache, bt, ctx, int(wl.kv_lens.max()),
                                 wl.softmax_scale)
     assert np.array_equal(bits(out), bits(ref))
+    expect_no_device_error(pkv)
+
+
+def test_prefill_step_graph_replay_matches_eager(pkv):
+    """Slot mapping, KV scatter and prefill of a chunked batch with prefix hits, captured once
+    and replayed: bit-identical to the eager calls, also after new Q/K/V values are written into
+    the captured buffers."""
+    wl = W.prefill_prefix(batch=8)
+    b = GpuBatch(wl, W.paged_values(wl))
+    out = torch.empty_like(b.q)
+    ws = torch.empty(max(pkv.pkv_prefill_workspace_size(wl.batch, wl.num_heads, wl.num_kv_heads, wl.head_dim,
+                                                        int(wl.q_lens.max())), 256),
+                     dtype=torch.uint8, device="cuda")
+    mq, mk = int(wl.q_lens.max()), int(wl.kv_lens.max())
+
+    def step():
+        b.run_slots_and_store(pkv, decode=False)
+        pkv.pkv_prefill_varlen(b.q, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables, mq, mk,
+                               wl.softmax_scale, out=out, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()                                        # first call on the device: set-up before capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    gen = torch.Generator(device="cuda").manual_seed(71)
+    for replay in range(2):
+        if replay:                                    # new values, same buffers
+            b.q.copy_(torch.randn(b.q.shape, generator=gen, device="cuda").to(torch.bfloat16))
+            b.k_new.copy_(torch.randn(b.k_new.shape, generator=gen, device="cuda").to(torch.bfloat16))
+            b.v_new.copy_(torch.randn(b.v_new.shape, generator=gen, device="cuda").to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        got = bits(out).copy()
+        b.run_slots_and_store(pkv, decode=False)
+        ref = pkv.pkv_prefill_varlen(b.q, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables, mq, mk,
+                                     wl.softmax_scale, workspace=ws)
+        assert np.array_equal(bits(ref), got)
     expect_no_device_error(pkv)
