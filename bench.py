@@ -615,6 +615,39 @@ def bench_long_decode(args, pkv, torch, peaks):
     return res
 
 
+def bench_decode_sweep(args, pkv, torch, peaks):
+    """The fused decode step across batch sizes and context lengths (every sequence of a batch
+    at the same length), each call timed cold: L2 flushed before it, events around it alone."""
+    flush = L2Flush(torch)
+    rows = []
+    for L in (512, 4096, 32768):
+        for B in (1, 4, 16, 64, 256):
+            if B * L * 4096 > 16e9:
+                continue
+            wl = W.build_workload(f"sweep-b{B}-l{L}", np.ones(B, np.int32), np.full(B, L, np.int32),
+                                  seed=3000 + B + L)
+            st = DecodeStep(pkv, torch, wl)
+            for _ in range(3):
+                st.layer(0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ts = []
+            for _ in range(20):
+                flush()
+                a.record()
+                st.layer(0)
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            ms = float(np.median(ts))
+            rows.append({"batch": B, "context": L, "call_us": ms * 1e3, "gbs": wl.kv_bytes_read / (ms * 1e-3) / 1e9,
+                         "frac_of_hbm": wl.kv_bytes_read / (ms * 1e-3) / 1e9 / peaks[0],
+                         "tok_per_s_per_layer": B / (ms * 1e-3)})
+            del st
+            torch.cuda.empty_cache()
+    return {"workload": "pkv_decode_append, batch x context grid, each sequence at the same length, "
+                        "L2 flushed before every call (median of 20)", "rows": rows}
+
+
 def bench_full_step(args, pkv, torch, peaks):
     wl = W.full_step()
     st = DecodeStep(pkv, torch, wl, layers=wl.num_layers)
@@ -701,7 +734,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-secondary", action="store_true", help="headline only")
     ap.add_argument("--parts", default="prefill,long,full,rope",
-                    help="secondary workloads to run: any of prefill,long,full,rope")
+                    help="secondary workloads to run: any of prefill,long,full,rope,sweep (sweep is opt-in)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args(argv)
@@ -732,7 +765,8 @@ def main(argv=None):
         # each part runs inside an NVTX range of its own name, so a profiler can select one
         # (ncu --nvtx --nvtx-include "full_step/")
         for key, part, fn in (("prefill", "prefill", bench_prefill), ("long", "long_decode", bench_long_decode),
-                              ("full", "full_step", bench_full_step), ("rope", "rope_store", bench_rope_store)):
+                              ("full", "full_step", bench_full_step), ("rope", "rope_store", bench_rope_store),
+                              ("sweep", "decode_sweep", bench_decode_sweep)):
             if key in parts:
                 torch.cuda.nvtx.range_push(part)
                 try:

@@ -9,9 +9,12 @@
 // * Work partition.  The KV of the batch is cut into 32-token chunks, ordered
 //   (sequence, KV head, chunk).  The persistent grid's W warps each take one
 //   contiguous run of floor((w+1)T/W) - floor(wT/W) chunks, so every warp
-//   streams the same number of bytes whatever the length mix.  A run that
-//   crosses a (sequence, KV head) boundary flushes a partial softmax state
-//   (running max m, sum l, unnormalised o) for each piece.
+//   streams the same number of bytes whatever the length mix.  A step with
+//   fewer than 4 chunks per warp uses only ceil(T/4) warps, so short
+//   sequences are not cut into single-chunk pieces that the combine must
+//   then merge one round trip after another.  A run that crosses a
+//   (sequence, KV head) boundary flushes a partial softmax state (running
+//   max m, sum l, unnormalised o) for each piece.
 // * Per-warp TMA pipeline.  Each warp owns STAGES shared-memory stages of
 //   one chunk of K and V (8 KiB each, 32 tokens x 256 B rows of one KV head,
 //   cut out of the [num_blocks, block_size, Hkv, 128] pool by a 4-D tensor
@@ -77,6 +80,14 @@ struct Params {
 };
 
 __device__ __forceinline__ int seq_chunks(const int32_t* prefix, int b) { return prefix[b + 1] - prefix[b]; }
+
+// Warps the run is cut over: all of them, unless that would leave fewer than KMIN chunks a
+// warp (a small step), where fewer, longer runs mean fewer pieces for the combine to merge.
+constexpr int KMIN = 4;
+__device__ __forceinline__ int run_warps(int total_warps, int64_t total) {
+    const int64_t w = (total + KMIN - 1) / KMIN;
+    return static_cast<int>(w < total_warps ? (w > 0 ? w : 1) : total_warps);
+}
 
 // floor(a * b / c) for non-negative operands; `narrow` (a * b known to fit in 32 bits) takes
 // the unsigned 32-bit divide instead of the much longer 64-bit one.
@@ -264,9 +275,10 @@ decode_splitk_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     }
 
     // ---- this warp's run of chunks
-    const int W = p.total_warps;
     const int gw = blockIdx.x * WARPS + warp;
     const int64_t total = static_cast<int64_t>(hkv) * prefix[p.batch];
+    const int W = run_warps(p.total_warps, total);
+    if (gw >= W) return;
     const bool narrow = total * W <= 0xffffffffll;
     const int64_t begin = mul_div(gw, total, W, narrow);
     const int64_t end = mul_div(gw + 1, total, W, narrow);
@@ -534,8 +546,8 @@ decode_combine_kernel(const Params p, int num_heads, uint16_t* __restrict__ out)
         if (h == 0 && lane == 0 && p.slot_out != nullptr) p.slot_out[b] = -1;   // nothing was written
         return;
     }
-    const int64_t W = p.total_warps;
     const int64_t total = static_cast<int64_t>(hkv) * plan_all;
+    const int64_t W = run_warps(p.total_warps, total);
     const int64_t start = static_cast<int64_t>(hkv) * plan_b + static_cast<int64_t>(g) * n;
     const int64_t last = start + n - 1;
     const bool narrow = total * W <= 0xffffffffll;
