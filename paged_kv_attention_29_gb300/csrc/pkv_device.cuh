@@ -217,38 +217,15 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive on an mbarrier once every previously issued tcgen05 op of this thread completes.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Warp-wide forms of the three calls above: every lane of a converged warp makes
-// the call and one lane chosen by elect.sync issues the instruction.  Issued this
-// way the operands stay warp-uniform, and one MMA costs the issuing warp about as
-// long as the tensor core takes to run it, where a lone lane inside a divergent
-// branch needs markedly longer.  The same lane is elected every time, so a
-// commit covers the MMAs of the earlier calls.
+// tcgen05 MMA issue, warp-wide: every lane of a converged warp makes the call and one
+// lane chosen by elect.sync issues the instruction.  Issued this way the operands stay
+// warp-uniform, and one MMA costs the issuing warp about as long as the tensor core takes
+// to run it, where a lone lane inside a divergent branch needs markedly longer.  The same
+// lane is elected every time, so a commit covers the MMAs of the earlier calls.
+//   mma_ss_warp      D[tmem] (+)= A[smem desc] * B[smem desc]
+//   mma_ts_warp      D[tmem] (+)= A[tmem] * B[smem desc]
+//   mma_commit_warp  arrive on an mbarrier once every earlier tcgen05 op of the issuing
+//                    lane has completed
 __device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
     asm volatile(
