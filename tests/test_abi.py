@@ -74,6 +74,12 @@ def test_host_argument_checks_return_before_launch(lib):
     assert lib.pkv_rope_store_kvcache(P, 0, P, 0, P, 1024, P, 1024, P, 4, 0, 8, 128, 0.0, P, P, P, 4, 256, P) == 1
     assert lib.pkv_rope_store_kvcache(P, 0, P, 0, P, 512, P, 1024, P, 4, 0, 8, 128, 1e6, P, P, P, 4, 256, P) == 1
     assert lib.pkv_rope_store_kvcache(P, 0, P, 0, P, 1024, P, 1024, P, 0, 0, 8, 128, 1e6, P, P, P, 4, 256, P) == 0
+    # decode_append: unsupported head_dim; a pointer that is not 16-byte aligned; zero batch is a no-op
+    assert lib.pkv_decode_append(P, P, P, P, P, P, 4, P, 2, 10, 16, 8, 64, 256, 4, 0.1, P, P, P, 0, P) == 2
+    odd = ctypes.c_void_p(8)        # non-null, 8-byte aligned only, never dereferenced
+    assert lib.pkv_decode_append(odd, odd, odd, odd, odd, odd, 4, odd, 2, 10, 16, 8, 128, 256, 4, 0.1, odd, P, P, 0,
+                                 P) == 2
+    assert lib.pkv_decode_append(P, P, P, P, P, P, 4, P, 0, 10, 16, 8, 128, 256, 4, 0.1, P, P, P, 0, P) == 0
     # zero-size calls are no-ops
     assert lib.pkv_store_kvcache(P, P, 0, 1024, 1024, P, P, P, 4, 256, 8, 128, P) == 0
     assert lib.pkv_sample(P, 0, 10, 10, P, 0, 0, P, P) == 0
