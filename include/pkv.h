@@ -258,7 +258,7 @@ PKV_API pkv_status pkv_decode_append(const pkv_bf16 *q, const pkv_bf16 *k_new, c
                              void *workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /*
- * Decode without any allocation.  The paper has no counterpart: this is a
+ * Decode without any allocation.  No step of the engine calls for it: this is a
  * library convenience for callers that cannot call cudaMalloc -- for example
  * a plugin inside a host runtime that owns all device memory and hands it only
  * its input and output buffers, or a service whose device-memory budget is
