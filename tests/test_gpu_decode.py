@@ -10,7 +10,7 @@ from pkv_testutil import GpuBatch, assert_attention_close, bits, expect_no_devic
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["tiny-decode", "decode-b64", "long-decode"])
+@pytest.mark.parametrize("name", ["tiny-decode", "decode-b64", "long-decode", "full-step"])
 def test_decode_configs_all_rows(pkv, name):
     """Write the new token's K/V through the slot mapping, then decode; every row vs the oracle."""
     wl = W.ALL[name]()
@@ -114,7 +114,7 @@ def test_decode_flags_block_id_outside_pool(pkv):
     assert code == 1 and info == 1
 
 
-@pytest.mark.parametrize("name", ["tiny-decode", "decode-b64", "long-decode"])
+@pytest.mark.parametrize("name", ["tiny-decode", "decode-b64", "long-decode", "full-step"])
 def test_decode_append_matches_oracle(pkv, name):
     """KV write fused into decode: pool bit-exact, slots bit-exact, output vs the fp64 oracle."""
     wl = W.ALL[name]()
