@@ -92,3 +92,24 @@ def test_binding_refuses_cpu_tensors(lib):
     pool = torch.zeros(2, 256, 8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         pkv.pkv_store_kvcache(x, x, torch.zeros(4, dtype=torch.int32), pool, pool)
+
+
+def test_readme_example_calls_the_binding_as_it_is():
+    """Every pkv.* call in the README's Python example names a binding function and passes
+    arguments its signature accepts."""
+    import ast
+    import inspect
+    import paged_kv_attention_29_gb300 as pkv
+    text = open(os.path.join(ROOT, "README.md")).read()
+    blocks = re.findall(r"```python\n(.*?)```", text, re.S)
+    assert blocks, "the README has no Python example"
+    calls = [n for b in blocks for n in ast.walk(ast.parse(b))
+             if isinstance(n, ast.Call) and isinstance(n.func, ast.Attribute)
+             and isinstance(n.func.value, ast.Name) and n.func.value.id == "pkv"]
+    assert len(calls) >= 5
+    for c in calls:
+        fn = getattr(pkv, c.func.attr)
+        sig = inspect.signature(fn)
+        args = [object()] * len(c.args)
+        kwargs = {k.arg: object() for k in c.keywords}
+        sig.bind(*args, **kwargs)        # raises TypeError on a wrong name or count
