@@ -39,7 +39,11 @@ import subprocess
 import sys
 import time
 
-import numpy as np
+# The CPU baseline reports how many threads the oracle's BLAS ran on; fix that number before
+# NumPy loads OpenBLAS (one thread unless the caller sets it), so the report is what ran.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -232,7 +236,7 @@ def run_reference(args):
         tot_bytes += oracle_decode_sample(wl, kc, vc, q, kn, vn, [(i * n_rows + j) % wl.batch for j in range(n_rows)])
     dt = time.perf_counter() - t0
     value = tot_bytes / dt / 1e9
-    threads = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS") or "1"
+    threads = os.environ["OPENBLAS_NUM_THREADS"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / max(1, args.steps) * 1e3, "higher_is_better": True,
@@ -780,7 +784,7 @@ def main(argv=None):
     cpu_baseline = None
     if rank == 0 and cpu_arrays is not None:
         gbs, rows, dt = time_oracle(wl, cpu_arrays, args.cpu_budget)
-        threads = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS") or "1"
+        threads = os.environ["OPENBLAS_NUM_THREADS"]
         cpu_baseline = {"value": gbs, "unit": "GB/s", "cores": int(threads), "kind": "oracle",
                         "sample": f"{rows} sequences of the batch-64 decode workload, one at a time "
                                   f"(KV scatter + fp64 gather-then-dense attention), {dt:.1f} s",
