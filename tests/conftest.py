@@ -17,7 +17,7 @@ def pytest_configure(config):
 
 @pytest.fixture(scope="session")
 def pkv():
-    """The CUDA library binding.  On a GPU machine a missing build is a hard failure."""
+    """The CUDA library binding.  On a machine with a CUDA device, a missing build is a hard failure."""
     import torch
     if not torch.cuda.is_available():
         pytest.fail("GPU test collected on a machine without CUDA")
