@@ -183,29 +183,28 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, block_size: int,
            scale: float) -> np.ndarray:
     """One decode token per sequence over ``context_lens[b]`` cached keys.
 
-    q: [B, Hq, d].  A sequence with no context gives a zero row."""
-    q = np.asarray(q)
-    out = np.zeros(q.shape, dtype=np.float64)
-    for b in range(q.shape[0]):
-        L = int(context_lens[b])
-        if L == 0:
-            continue
-        K = gather_sequence(k_cache, block_tables[b], L, block_size)
-        V = gather_sequence(v_cache, block_tables[b], L, block_size)
-        out[b] = attention_dense(q[b:b + 1], K, V, scale)[0]
-    return out
+    q: [B, Hq, d].  A sequence with no context gives a zero row.  Every
+    sequence is :func:`decode_rows` of its own row."""
+    return decode_rows(q, k_cache, v_cache, block_tables, context_lens, block_size, scale,
+                       range(np.asarray(q).shape[0]))
 
 
 def decode_rows(q, k_cache, v_cache, block_tables, context_lens, block_size: int,
                 scale: float, rows) -> np.ndarray:
-    """:func:`decode` for the listed sequences only (sampled checks at full size)."""
+    """Decode attention for the listed sequences, in the listed order.
+
+    Row ``i`` of the result is sequence ``rows[i]``: its query token
+    ``q[rows[i]]`` attends over the first ``context_lens[rows[i]]`` positions
+    of its paged context (atlas fig. 21, with the KV of the newest token
+    already written).  A sequence with no context gives a zero row."""
     rows = list(rows)
-    out = np.zeros((len(rows),) + tuple(np.asarray(q).shape[1:]), dtype=np.float64)
+    q = np.asarray(q)
+    out = np.zeros((len(rows),) + tuple(q.shape[1:]), dtype=np.float64)
     for i, b in enumerate(rows):
         L = int(context_lens[b])
         if L == 0:
             continue
         K = gather_sequence(k_cache, block_tables[b], L, block_size)
         V = gather_sequence(v_cache, block_tables[b], L, block_size)
-        out[i] = attention_dense(np.asarray(q)[b:b + 1], K, V, scale)[0]
+        out[i] = attention_dense(q[b:b + 1], K, V, scale)[0]
     return out

@@ -18,14 +18,13 @@ Readings where the pages are silent (the CUDA path follows the same ones):
 """
 from __future__ import annotations
 
-import math
-
 import numpy as np
 
 
-def rotate_pair(a: float, b: float, angle: float):
-    """The atlas fig. 19 picture: one 2-D pair turned by `angle`."""
-    c, s = math.cos(angle), math.sin(angle)
+def rotate_pair(a, b, angle):
+    """The atlas fig. 19 picture: the 2-D pair (a, b) turned counter-clockwise
+    by ``angle`` radians.  Works elementwise on arrays of pairs."""
+    c, s = np.cos(angle), np.sin(angle)
     return a * c - b * s, b * c + a * s
 
 
@@ -40,10 +39,8 @@ def rope(x, positions, base: float) -> np.ndarray:
     half = d // 2
     inv_freq = np.array([base ** (-2.0 * i / d) for i in range(half)])
     angle = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]   # [N, d/2]
-    c = np.cos(angle)[:, None, :]
-    s = np.sin(angle)[:, None, :]
-    a, b = x[..., :half], x[..., half:]
-    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+    a_rot, b_rot = rotate_pair(x[..., :half], x[..., half:], angle[:, None, :])
+    return np.concatenate([a_rot, b_rot], axis=-1)
 
 
 def rope_store_kvcache(q, k_cache, v_cache, k, v, positions, slots, block_size: int, base: float):

@@ -276,6 +276,32 @@ def test_decode_zero_context_is_zero_row():
     assert np.all(out[1] == 0) and np.any(out[0] != 0)
 
 
+def test_decode_rows_selects_rows_in_the_listed_order():
+    """decode_rows(rows)[i] is sequence rows[i] attending its paged context: checked against
+    torch's SDPA on the allocator-walk copy of each listed sequence (a library reference that
+    shares nothing with the oracle's gather), with the rows listed out of order, one of them
+    twice and one with no context (its row is zero).  Catches indexing q or the tables by the
+    output position instead of the sequence."""
+    rng = np.random.default_rng(41)
+    bs = 4
+    kv_lens = np.array([5, 0, 11, 2, 8])
+    tables, kc, vc = _random_paged(rng, np.maximum(kv_lens, 1), bs, 12)
+    q = rng.standard_normal((5, 4, 8))
+    rows = [4, 1, 2, 0, 4]
+    out = pa.decode_rows(q, kc, vc, tables, kv_lens, bs, 0.35, rows)
+    assert out.shape == (len(rows), 4, 8)
+    for i, b in enumerate(rows):
+        L = int(kv_lens[b])
+        if L == 0:
+            assert np.all(out[i] == 0)
+            continue
+        K = _contiguous(kc, tables[b], L, bs)
+        V = _contiguous(vc, tables[b], L, bs)
+        ref = _sdpa_causal(np.concatenate([np.zeros((L - 1, 4, 8)), q[b:b + 1]]), K, V, 0.35)[-1]
+        np.testing.assert_allclose(out[i], ref, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(out, pa.decode(q, kc, vc, tables, kv_lens, bs, 0.35)[rows])
+
+
 # ---------------------------------------------------------------------------
 # Philox noise and the exponential race
 # ---------------------------------------------------------------------------
@@ -332,6 +358,24 @@ def test_race_invariances():
     assert np.array_equal(sm.exponential_race(logits * 4.0, T * 4.0, e)[0], ids)
     ids_hot, _ = sm.exponential_race(logits, T * 50, e)
     assert np.any(ids_hot != ids)
+
+
+def test_race_margin_closed_form():
+    """Hand-picked 3-token rows where the race's two best ratios are known exactly.
+
+    Row 0: logits ln(1), ln(2), ln(3) at T = 1, so p = (1, 2, 3) / 6; noise (1, 1, 2)
+    gives p/e = (1, 2, 1.5) / 6: winner 1, margin ln(2 / 1.5) = ln(4/3).
+    Row 1: logits (0, ln 3, ln 2) * 0.5 at T = 0.5 (p = (1, 3, 2) / 6); noise (0.25, 2, 1)
+    gives p/e = (4, 1.5, 2) / 6: winner 0, margin ln(4 / 2) = ln 2, the second best not
+    adjacent to the winner.  A margin taken against the wrong entry, from p*e, or without
+    the temperature fails one of them."""
+    logits = np.array([[0.0, math.log(2.0), math.log(3.0)],
+                       [0.0, 0.5 * math.log(3.0), 0.5 * math.log(2.0)]])
+    T = np.array([1.0, 0.5])
+    e = np.array([[1.0, 1.0, 2.0], [0.25, 2.0, 1.0]])
+    ids, margin = sm.exponential_race(logits, T, e)
+    assert ids.tolist() == [1, 0]
+    np.testing.assert_allclose(margin, [math.log(4.0 / 3.0), math.log(2.0)], rtol=0, atol=1e-14)
 
 
 def test_race_frequencies_match_softmax():
@@ -415,3 +459,14 @@ def test_rope_pairing_and_frequencies_closed_form():
         out = rp.rope(np.array([[[1.0, 1.0, 0.0, 0.0]]]), [p], base=100.0)[0, 0]
         np.testing.assert_allclose(out, [math.cos(p), math.cos(0.1 * p), math.sin(p), math.sin(0.1 * p)],
                                    rtol=0, atol=1e-13)
+
+
+def test_rotate_pair_is_the_counter_clockwise_rotation():
+    """rotate_pair, the figure's single pair: a quarter turn takes (1, 0) to (0, 1) and (0, 1) to
+    (-1, 0); a half turn negates; any turn keeps the length; arrays of pairs turn elementwise."""
+    np.testing.assert_allclose(rp.rotate_pair(1.0, 0.0, math.pi / 2), (0.0, 1.0), atol=1e-15)
+    np.testing.assert_allclose(rp.rotate_pair(0.0, 1.0, math.pi / 2), (-1.0, 0.0), atol=1e-15)
+    np.testing.assert_allclose(rp.rotate_pair(0.3, -0.8, math.pi), (-0.3, 0.8), atol=1e-15)
+    a, b = rp.rotate_pair(np.array([3.0, 0.5]), np.array([4.0, -2.0]), np.array([0.7, 2.9]))
+    np.testing.assert_allclose(np.hypot(a, b), [5.0, math.hypot(0.5, 2.0)], rtol=1e-15)
+    np.testing.assert_allclose(a[0], 3.0 * math.cos(0.7) - 4.0 * math.sin(0.7), rtol=1e-15)
