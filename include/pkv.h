@@ -271,7 +271,10 @@ PKV_API pkv_status pkv_decode_append(const pkv_bf16 *q, const pkv_bf16 *k_new, c
  * PKV_ERR_UNSUPPORTED (it fits up to 427 sequences with 8 KV heads on a
  * 152-SM GPU).
  * The first call on each device looks up the array's device address; make
- * that first call before any stream capture.  All calls share the array and
+ * that first call before any stream capture.  The address is kept for the
+ * process: after a cudaDeviceReset this entry point must not be called again
+ * (the same holds for every call of the library, whose per-device error word
+ * and kernel set-up are kept the same way).  All calls share the array and
  * it keeps the last call's contents (nothing in it needs to start at zero);
  * calls that overlap on the GPU race on it and must be serialised.
  */

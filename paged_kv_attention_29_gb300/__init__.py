@@ -132,6 +132,44 @@ def _check(t: torch.Tensor, name: str, dtype, ndim=None, contiguous=True):
         raise ValueError(f"{name} must be contiguous")
 
 
+class _on_device:
+    """Run a library call with the tensors' device current.
+
+    The library launches on the current device and looks up per-device state
+    (error word, kernel attributes, scratch) there, so every tensor of a call
+    must sit on one device and that device must be current.  Makes it current
+    for the duration of the call when it is not already; a stream given by the
+    caller must belong to it."""
+
+    __slots__ = ("dev", "prev")
+
+    def __init__(self, *tensors, stream=None):
+        dev = None
+        for t in tensors:
+            if t is None:
+                continue
+            if dev is None:
+                dev = t.device
+            elif t.device != dev:
+                raise ValueError(f"all tensors of a call must be on one device (got {dev} and {t.device})")
+        self.dev = dev.index if dev is not None else torch.cuda.current_device()
+        if stream is not None and stream.device.index != self.dev:
+            raise ValueError(f"stream is on cuda:{stream.device.index}, tensors on cuda:{self.dev}")
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.dev:
+            self.prev = cur
+            torch.cuda.set_device(self.dev)
+        return self
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
+
+
 def _raise(status: int, where: str):
     if status != 0:
         raise PkvError(status, where)
@@ -160,7 +198,8 @@ def pkv_slot_mapping(block_tables: torch.Tensor, num_blocks: int, block_size: in
         if t is not None:
             _check(t, name, torch.int32, 1)
     num_seqs = block_tables.shape[0]
-    _raise(load().pkv_slot_mapping(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(context_lens), _ptr(block_tables),
+    with _on_device(block_tables, slot_mapping, cu_seqlens_q, cu_seqlens_k, context_lens, stream=stream):
+        _raise(load().pkv_slot_mapping(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(context_lens), _ptr(block_tables),
                                    block_tables.shape[1], num_seqs, slot_mapping.shape[0], block_size, num_blocks,
                                    _ptr(slot_mapping), _stream(stream)), "pkv_slot_mapping")
     return slot_mapping
@@ -187,9 +226,10 @@ def pkv_store_kvcache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
     n = k.shape[0]
     if v.shape[0] != n or slot_mapping.shape[0] != n:
         raise ValueError("k, v and slot_mapping disagree on the token count")
-    _raise(load().pkv_store_kvcache(_ptr(k), _ptr(v), n, k.stride(0), v.stride(0), _ptr(slot_mapping),
-                                    _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, _stream(stream)),
-           "pkv_store_kvcache")
+    with _on_device(k, v, slot_mapping, k_cache, v_cache, stream=stream):
+        _raise(load().pkv_store_kvcache(_ptr(k), _ptr(v), n, k.stride(0), v.stride(0), _ptr(slot_mapping),
+                                        _ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, _stream(stream)),
+               "pkv_store_kvcache")
 
 
 def pkv_rope_store_kvcache(q: Optional[torch.Tensor], k: torch.Tensor, v: torch.Tensor, positions: torch.Tensor,
@@ -225,12 +265,13 @@ def pkv_rope_store_kvcache(q: Optional[torch.Tensor], k: torch.Tensor, v: torch.
             raise ValueError("q_out must match q's shape with contiguous rows")
     elif q_out is not None:
         raise ValueError("q_out given without q")
-    _raise(load().pkv_rope_store_kvcache(_ptr(q), q.stride(0) if q is not None else 0, _ptr(q_out),
-                                         q_out.stride(0) if q_out is not None else 0, _ptr(k), k.stride(0),
-                                         _ptr(v), v.stride(0), _ptr(positions), n, hq, hkv, d, float(rope_base),
-                                         _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb, bs,
-                                         _stream(stream)),
-           "pkv_rope_store_kvcache")
+    with _on_device(q, q_out, k, v, positions, slot_mapping, k_cache, v_cache, stream=stream):
+        _raise(load().pkv_rope_store_kvcache(_ptr(q), q.stride(0) if q is not None else 0, _ptr(q_out),
+                                             q_out.stride(0) if q_out is not None else 0, _ptr(k), k.stride(0),
+                                             _ptr(v), v.stride(0), _ptr(positions), n, hq, hkv, d, float(rope_base),
+                                             _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb, bs,
+                                             _stream(stream)),
+               "pkv_rope_store_kvcache")
     return q_out
 
 
@@ -263,10 +304,11 @@ def pkv_prefill_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
         n = pkv_prefill_workspace_size(num_seqs, hq, hkv, d, int(max_seqlen_q))
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _raise(load().pkv_prefill_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                                     _ptr(block_tables), block_tables.shape[1], num_seqs, total_q, int(max_seqlen_q),
-                                     int(max_seqlen_k), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
-                                     _ptr(workspace), ws_bytes, _stream(stream)), "pkv_prefill_varlen")
+    with _on_device(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, out, workspace, stream=stream):
+        _raise(load().pkv_prefill_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                         _ptr(block_tables), block_tables.shape[1], num_seqs, total_q, int(max_seqlen_q),
+                                         int(max_seqlen_k), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
+                                         _ptr(workspace), ws_bytes, _stream(stream)), "pkv_prefill_varlen")
     return out
 
 
@@ -301,10 +343,11 @@ def pkv_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, bl
     if workspace is None:
         workspace = decode_workspace(batch, hq, hkv, d, q.device)
     _check(workspace, "workspace", torch.uint8, 1)
-    _raise(load().pkv_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
-                             _ptr(context_lens), batch, int(max_context_len), hq, hkv, d, bs, nb,
-                             float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "pkv_decode")
+    with _on_device(q, k_cache, v_cache, block_tables, context_lens, out, workspace, stream=stream):
+        _raise(load().pkv_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+                                 _ptr(context_lens), batch, int(max_context_len), hq, hkv, d, bs, nb,
+                                 float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)),
+               "pkv_decode")
     return out
 
 
@@ -335,11 +378,13 @@ def pkv_decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     if workspace is None:
         workspace = decode_workspace(batch, hq, hkv, d, q.device)
     _check(workspace, "workspace", torch.uint8, 1)
-    _raise(load().pkv_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), batch,
-                                    int(max_context_len), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
-                                    _ptr(slot_mapping), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "pkv_decode_append")
+    with _on_device(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out, slot_mapping, workspace,
+                    stream=stream):
+        _raise(load().pkv_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), batch,
+                                        int(max_context_len), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
+                                        _ptr(slot_mapping), _ptr(workspace), workspace.numel(), _stream(stream)),
+               "pkv_decode_append")
     return out
 
 
@@ -366,13 +411,19 @@ class DecodeAppendCall:
                       block_tables.shape[1], _ptr(context_lens), batch, int(max_context_len), hq, hkv, d, bs, nb,
                       float(softmax_scale), _ptr(out), _ptr(slot_mapping), _ptr(workspace), workspace.numel())
         self._stream = None if stream is None else _stream(stream)   # None: the current stream per call
+        self._dev = q.device.index
         self.out = out
 
     def __call__(self, stream=None) -> torch.Tensor:
         """Launch on `stream`, else on the stream given at construction, else on the current stream
-        (so a call made while a CUDA graph is being captured is captured)."""
-        s = _stream(stream) if stream is not None else (self._stream if self._stream is not None else _stream())
-        _raise(self._fn(*self._args, s), "pkv_decode_append")
+        of the buffers' device (so a call made while a CUDA graph is being captured is captured)."""
+        if stream is None and torch.cuda.current_device() == self._dev:
+            s = self._stream if self._stream is not None else _stream()
+            _raise(self._fn(*self._args, s), "pkv_decode_append")
+            return self.out
+        with _on_device(self.out, stream=stream):
+            s = _stream(stream) if stream is not None else (self._stream if self._stream is not None else _stream())
+            _raise(self._fn(*self._args, s), "pkv_decode_append")
         return self.out
 
 
@@ -391,10 +442,11 @@ def pkv_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
     batch, hq, dq = q.shape
     if dq != d or context_lens.shape[0] != batch or block_tables.shape[0] != batch or out.shape != q.shape:
         raise ValueError("q, out, context_lens and block_tables disagree")
-    _raise(load().pkv_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
-                                     block_tables.shape[1], _ptr(context_lens), batch, int(max_context_len), hq,
-                                     hkv, d, bs, nb, float(softmax_scale), _ptr(out), _stream(stream)),
-           "pkv_decode_noalloc")
+    with _on_device(q, k_cache, v_cache, block_tables, context_lens, out, stream=stream):
+        _raise(load().pkv_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                         block_tables.shape[1], _ptr(context_lens), batch, int(max_context_len), hq,
+                                         hkv, d, bs, nb, float(softmax_scale), _ptr(out), _stream(stream)),
+               "pkv_decode_noalloc")
     return out
 
 
@@ -409,9 +461,10 @@ def pkv_sample(logits: torch.Tensor, temperatures: torch.Tensor, seed: int, offs
     if out_ids is None:
         out_ids = torch.empty(batch, dtype=torch.int64, device=logits.device)
     _check(out_ids, "out_ids", torch.int64, 1)
-    _raise(load().pkv_sample(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures),
-                             int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(out_ids),
-                             _stream(stream)), "pkv_sample")
+    with _on_device(logits, temperatures, out_ids, stream=stream):
+        _raise(load().pkv_sample(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures),
+                                 int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(out_ids),
+                                 _stream(stream)), "pkv_sample")
     return out_ids
 
 
@@ -430,8 +483,9 @@ def pkv_sample_dev(logits: torch.Tensor, temperatures: torch.Tensor, seed_offset
     if out_ids is None:
         out_ids = torch.empty(batch, dtype=torch.int64, device=logits.device)
     _check(out_ids, "out_ids", torch.int64, 1)
-    _raise(load().pkv_sample_dev(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures), _ptr(seed_offset),
-                                 _ptr(out_ids), _stream(stream)), "pkv_sample_dev")
+    with _on_device(logits, temperatures, seed_offset, out_ids, stream=stream):
+        _raise(load().pkv_sample_dev(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures), _ptr(seed_offset),
+                                     _ptr(out_ids), _stream(stream)), "pkv_sample_dev")
     return out_ids
 
 
@@ -441,7 +495,8 @@ WAIT_CHECK_INFO = 0x5741
 def pkv_check_wait_timeout(stream=None) -> None:
     """Run the failure-path check: one wait that nothing completes gives up after its limit
     (about 2 s) and records (DEVERR timeout, WAIT_CHECK_INFO); read it with pkv_get_device_error."""
-    _raise(load().pkv_check_wait_timeout(_stream(stream)), "pkv_check_wait_timeout")
+    with _on_device(stream=stream):
+        _raise(load().pkv_check_wait_timeout(_stream(stream)), "pkv_check_wait_timeout")
 
 
 def pkv_get_device_error(clear: bool = True):

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <math.h>
+#include <atomic>
 #include <mutex>
 
 #include "pkv_device.cuh"
@@ -41,6 +42,9 @@ DeviceCache* current_cache() {
     }
     return &c;
 }
+
+std::atomic<bool> g_setup_done[kMaxDevices][kNumSetupKeys];
+std::mutex g_setup_mu;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -90,6 +94,18 @@ int* device_error_word() {
 int sm_count() {
     DeviceCache* c = current_cache();
     return c ? c->sms : 0;
+}
+
+bool setup_once(SetupKey key, bool (*setup)()) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::atomic<bool>& done = g_setup_done[dev][key];
+    if (done.load(std::memory_order_acquire)) return true;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (done.load(std::memory_order_relaxed)) return true;
+    if (!setup()) return false;
+    done.store(true, std::memory_order_release);
+    return true;
 }
 
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,

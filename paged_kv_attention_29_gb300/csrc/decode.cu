@@ -689,18 +689,14 @@ pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream) {
     p.slot_out = a.slot_out;
 
     const size_t smem = dynamic_smem_bytes(a.batch);
-    static int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        const int max_smem = static_cast<int>(dynamic_smem_bytes(MAX_BATCH));
-        if (cudaFuncSetAttribute(decode_splitk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(decode_splitk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-                cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured_device = dev;
-    }
+    if (!setup_once(kSetupDecode, [] {
+            const int max_smem = static_cast<int>(dynamic_smem_bytes(MAX_BATCH));
+            return cudaFuncSetAttribute(decode_splitk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        max_smem) == cudaSuccess &&
+                   cudaFuncSetAttribute(decode_splitk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        max_smem) == cudaSuccess;
+        }))
+        return PKV_ERR_CUDA;
     // both launches are programmatic dependents of what precedes them in the stream; each kernel
     // waits (griddepcontrol.wait) for its predecessor's completion before touching global memory
     cudaLaunchAttribute attr[1];

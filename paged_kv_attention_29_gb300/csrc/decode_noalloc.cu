@@ -12,11 +12,18 @@
 // The array is file-scope device memory of a fixed size: every GPU that loads
 // the library holds it until the process exits.  Its device address is looked
 // up once per device, on that device's first call (with the device current),
-// so make that first call before any stream capture.  All calls share the
-// array and it keeps the last call's contents; the decode kernels write every
-// byte they later read, so nothing has to be cleared between calls.  Calls
-// that overlap on the GPU (two streams, two host threads) race on the array
-// and must be serialised by the caller.
+// so make that first call before any stream capture.  The cached address
+// belongs to the device's current context: it does not survive a
+// cudaDeviceReset (or any teardown of the primary context), after which this
+// entry point must not be called again in the same process.
+//
+// All calls share the array and it keeps the last call's contents.  Nothing
+// in it needs to start at any particular value: the split-K kernel writes the
+// chunk plan and every piece state before the combine reads them, and where
+// the combine loads the state of a piece slot that no warp wrote this call
+// (its batched loads run ahead of the ownership test), it discards the value
+// unused.  Calls that overlap on the GPU (two streams, two host threads) race
+// on the array and must be serialised by the caller.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -20,6 +20,12 @@ int* device_error_word();
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// One-time set-up of kernel attributes, per device.  Runs `setup` with the
+// current device once (thread-safe; a failed set-up is retried on the next
+// call) and returns whether the set-up for `key` has succeeded on this device.
+enum SetupKey { kSetupDecode = 0, kSetupPrefill, kSetupRopeStore, kNumSetupKeys };
+bool setup_once(SetupKey key, bool (*setup)());
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, void* base,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,

@@ -27,14 +27,16 @@
 // exp2, a packed fp32x2 add for the row sum and one bf16x2 pack per two; the
 // mask is applied only on tiles the diagonal crosses.
 //
-// Persistent CTAs (one per SM) walk units in a static snake order over a list
-// that a one-CTA plan kernel sorts by cost (the longer tile's KV tiles) and leaves in the
-// workspace; the two launches are chained with programmatic dependent launch
-// so this kernel's set-up overlaps the plan.
+// Persistent CTAs (one per SM) take units from a list that a one-CTA plan
+// kernel sorts by cost (the longer tile's KV tiles, costliest first) and leaves
+// in the workspace: each CTA's producer claims the next unit with an atomic
+// increment when its current unit starts.  The two launches are chained with
+// programmatic dependent launch so this kernel's set-up overlaps the plan.
 //
 // Warps 0-3: softmax of tile A (TMEM lanes 0-127), warps 4-7: tile B; warp 8:
-// TMA producer; warp 9: TMEM allocation and the single MMA-issuing thread;
-// warps 10-11 only complete the third warpgroup for the register split.
+// TMA producer; warp 9: TMEM allocation and MMA issue (the whole warp runs the
+// loop, one lane elected per tcgen05 instruction); warps 10-11 only complete
+// the third warpgroup for the register split.
 #include <algorithm>
 
 #include "pkv_device.cuh"
@@ -743,21 +745,19 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
     p.err = err;
 
-    static int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        if (cudaFuncSetAttribute(prefill_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-                cudaSuccess)
-            return PKV_ERR_CUDA;
-        // the setmaxnreg split inside the kernel needs this many registers per thread at launch
+    if (!setup_once(kSetupPrefill, [] {
+            return cudaFuncSetAttribute(prefill_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES) == cudaSuccess &&
+                   cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        200 * 1024) == cudaSuccess;
+        }))
+        return PKV_ERR_CUDA;
+    // the setmaxnreg split inside the kernel needs this many registers per thread at launch
+    static const int launch_regs = [] {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, prefill_fa_kernel) != cudaSuccess) return PKV_ERR_CUDA;
-        if (fa.numRegs < static_cast<int>(kMinLaunchRegs)) return PKV_ERR_UNSUPPORTED;
-        configured_device = dev;
-    }
+        return cudaFuncGetAttributes(&fa, prefill_fa_kernel) == cudaSuccess ? fa.numRegs : -1;
+    }();
+    if (launch_regs < static_cast<int>(kMinLaunchRegs)) return PKV_ERR_UNSUPPORTED;
     prefill_plan_kernel<<<1, 1024, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.max_blocks, a.block_size,
                                                         max_cost, static_cast<uint4*>(a.workspace), err);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;

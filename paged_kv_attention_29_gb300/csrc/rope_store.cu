@@ -242,16 +242,12 @@ cudaError_t launch_rope_store(const RopeStoreArgs& a, int64_t n_tokens, int* err
     const int64_t stage = (a.q ? a.num_heads * 256 : 0) + 4 * a.kv_row;
     if (a.head_dim == 128 && stage <= kMaxStageBytes) {
         const size_t smem = static_cast<size_t>(kStages) * stage + 3 * kStages * 8;
-        static int configured_device = -1;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (configured_device != dev) {
-            const cudaError_t e = cudaFuncSetAttribute(rope_store_staged_kernel,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(kStages * kMaxStageBytes + 3 * kStages * 8));
-            if (e != cudaSuccess) return e;
-            configured_device = dev;
-        }
+        if (!setup_once(kSetupRopeStore, [] {
+                return cudaFuncSetAttribute(rope_store_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(kStages * kMaxStageBytes + 3 * kStages * 8)) ==
+                       cudaSuccess;
+            }))
+            return cudaErrorUnknown;
         const int64_t grid = std::min<int64_t>(n_tokens, 2LL * sm_count());
         rope_store_staged_kernel<<<static_cast<unsigned>(grid), kStagedThreads, smem, stream>>>(a, n_tokens, err);
         return cudaGetLastError();

@@ -65,8 +65,8 @@ def test_store_kvcache_bit_exact(pkv, name):
 
 @pytest.mark.parametrize("n", [3, 2048])
 def test_store_skips_padding_and_flags_out_of_pool(pkv, n):
-    """Slot -1 (padding) is skipped and a slot past the pool is flagged; 2048 tokens take the
-    staged bulk-copy path, 3 the one-CTA-per-token path."""
+    """Slot -1 (padding) is skipped and a slot past the pool is flagged, for a handful of
+    tokens and for a prefill-sized batch of 2048."""
     nb, bs = 16, 256
     g = torch.Generator().manual_seed(51)
     k = torch.randn(n, 8, 128, generator=g).to(torch.bfloat16).cuda()
