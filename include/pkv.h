@@ -30,8 +30,10 @@
  *   bf16, one pool per layer for K and one for V.  Block tables are int32
  *   [num_seqs, max_blocks_per_seq], row s listing sequence s's physical block
  *   ids in logical order, padded with -1.  Supported: head_dim = 128,
- *   block_size a multiple of 256, num_heads = 2 * num_kv_heads (two query
- *   heads share each KV head, as in Qwen3-0.6B); anything else returns
+ *   block_size a multiple of 256, and num_heads = G * num_kv_heads with a
+ *   group size G of 1, 2, 4 or 8 (MHA, and GQA with 2, 4 or 8 query heads
+ *   sharing each KV head -- Visual atlas fig. 18; Qwen3-0.6B has G = 2);
+ *   query head h reads KV head h / G.  Anything else returns
  *   PKV_ERR_UNSUPPORTED.
  * - bf16 tensors are passed as pkv_bf16 (the raw 16-bit pattern).
  *
@@ -217,6 +219,7 @@ PKV_API pkv_status pkv_prefill_varlen(const pkv_bf16 *q, const pkv_bf16 *k_cache
  * batch <= 4096 (PKV_ERR_UNSUPPORTED above, before any launch).
  * The work is split over the GPU's warps into equal runs of KV; partial
  * softmax states are merged in a fixed order, so results are deterministic.
+ * softmax_scale must be a positive finite number (PKV_ERR_INVALID_ARG).
  */
 PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
                                  int32_t head_dim);

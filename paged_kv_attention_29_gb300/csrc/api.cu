@@ -67,8 +67,8 @@ EncodeTiledFn encode_fn() {
 cudaStream_t as_stream(pkv_stream_t s) { return static_cast<cudaStream_t>(s); }
 
 bool supported_shape(int num_heads, int num_kv_heads, int head_dim, int block_size) {
-    return head_dim == kHeadDim && num_kv_heads > 0 && num_heads == kGroup * num_kv_heads &&
-           block_size > 0 && block_size % kBlockQuantum == 0;
+    return head_dim == kHeadDim && group_log2(num_heads, num_kv_heads) >= 0 && block_size > 0 &&
+           block_size % kBlockQuantum == 0;
 }
 
 // One thread waits on a barrier that nothing completes, through the bounded wait all the
@@ -89,6 +89,14 @@ __global__ void wait_check_kernel(int* err) {
 int* device_error_word() {
     DeviceCache* c = current_cache();
     return c ? c->err : nullptr;
+}
+
+int group_log2(int num_heads, int num_kv_heads) {
+    if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads) return -1;
+    const int g = num_heads / num_kv_heads;
+    for (int lg = 0; lg <= kMaxLogGroup; ++lg)
+        if (g == (1 << lg)) return lg;
+    return -1;
 }
 
 int sm_count() {
@@ -243,7 +251,7 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t n
                                   int32_t head_dim, int32_t max_seqlen_q) {
     if (num_seqs < 0 || max_seqlen_q < 0 || !supported_shape(num_heads, num_kv_heads, head_dim, kBlockQuantum))
         return 0;
-    return prefill_workspace_bytes(num_seqs, max_seqlen_q);
+    return prefill_workspace_bytes(num_seqs, max_seqlen_q, group_log2(num_heads, num_kv_heads));
 }
 
 pkv_status pkv_prefill_varlen(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
@@ -296,7 +304,7 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_k
     if (batch < 0 || !supported_shape(num_heads, num_kv_heads, head_dim, kBlockQuantum)) return 0;
     const int W = decode_total_warps();
     if (W <= 0) return 0;
-    return decode_workspace_bytes(batch, num_kv_heads, W);
+    return decode_workspace_bytes(batch, num_kv_heads, group_log2(num_heads, num_kv_heads), W);
 }
 
 pkv_status pkv_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
@@ -308,7 +316,7 @@ pkv_status pkv_decode(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16
                       pkv_stream_t stream) {
     (void)max_context_len;
     if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
-        !(softmax_scale == softmax_scale))
+        !(softmax_scale > 0.f) || softmax_scale == INFINITY)
         return PKV_ERR_INVALID_ARG;
     if (!supported_shape(num_heads, num_kv_heads, head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
@@ -346,7 +354,7 @@ pkv_status pkv_decode_append(const pkv_bf16* q, const pkv_bf16* k_new, const pkv
                              int32_t* slot_mapping, void* workspace, size_t workspace_bytes,
                              pkv_stream_t stream) {
     if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
-        !(softmax_scale == softmax_scale))
+        !(softmax_scale > 0.f) || softmax_scale == INFINITY)
         return PKV_ERR_INVALID_ARG;
     if (!supported_shape(num_heads, num_kv_heads, head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;

@@ -11,8 +11,11 @@
 namespace pkv {
 
 constexpr int kHeadDim = 128;
-constexpr int kGroup = 2;            // query heads per KV head
+constexpr int kMaxLogGroup = 3;      // query heads per KV head: 1, 2, 4 or 8
 constexpr int kBlockQuantum = 256;   // block_size must be a multiple of this
+
+// log2(num_heads / num_kv_heads) when that ratio is 1, 2, 4 or 8; otherwise -1.
+int group_log2(int num_heads, int num_kv_heads);
 
 // Device address of the current device's error word (int[2]); nullptr on failure.
 int* device_error_word();
@@ -88,7 +91,7 @@ struct DecodeArgs {
 };
 
 int decode_total_warps();                                  // warps the decode grid runs
-size_t decode_workspace_bytes(int batch, int num_kv_heads, int total_warps);
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int log_group, int total_warps);
 pkv_status launch_decode(const DecodeArgs& a, int* err, cudaStream_t stream);
 
 // ---- a3 ---------------------------------------------------------------------
@@ -114,7 +117,8 @@ struct PrefillArgs {
     size_t workspace_bytes;
 };
 
-size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q);
+// log_group = log2(num_heads / num_kv_heads)
+size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q, int log_group);
 pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream);
 
 // ---- a5 ---------------------------------------------------------------------

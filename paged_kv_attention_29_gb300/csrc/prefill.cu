@@ -6,9 +6,11 @@
 // of a chunk sees keys j <= i + k_len - q_len), fig. 18 (two query heads share
 // a K/V head), fig. 22 (blockwise evaluation without materialising scores).
 //
-// Work unit: 128 query tokens of one sequence x one KV head g, split into two
-// 128-row tiles A and B (64 tokens x the 2 query heads of the group each, so
-// both heads read one K/V tile).  Per unit and 128-key tile j:
+// Work unit: 256 / G query tokens of one sequence x one KV head g, split into
+// two 128-row tiles A and B (128 / G tokens x the G query heads of the group
+// each, so all G heads read one K/V tile; G = num_heads / num_kv_heads is 1, 2,
+// 4 or 8, row r of a tile being token r / G, head G g + r % G).  Per unit and
+// 128-key tile j:
 //
 //   S_X(j) = Q_X K_j^T      tcgen05.mma M=128 N=128, 8 x K=16, fp32 in TMEM
 //   P_X(j)                  masked online softmax by warpgroup X, bf16 over S_X
@@ -46,10 +48,7 @@ namespace pkv {
 namespace {
 
 constexpr int D = kHeadDim;
-constexpr int G = kGroup;
-constexpr int QTOK = 64;                  // tokens per 128-row tile
-constexpr int UNIT_TOK = 2 * QTOK;        // tokens per unit (tiles A and B)
-constexpr int ROWS = QTOK * G;            // MMA M
+constexpr int ROWS = 128;                 // MMA M: rows of a tile, (128 / G tokens) x (G heads)
 constexpr int KT = 128;                   // keys per KV tile
 constexpr int HALF_BYTES = ROWS * 64 * 2; // one 128B-swizzled box: 128 rows x 64 dims = 16 KiB
 constexpr int TILE_BYTES = 2 * HALF_BYTES;
@@ -98,6 +97,7 @@ struct Params {
     int max_blocks;
     int num_heads;
     int num_kv_heads;
+    int lg;                   // log2 of the group size G
     int block_size;
     int num_blocks;
     float scale_log2;
@@ -143,10 +143,10 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) { return smem_desc(addr, 16, 1024, 2); }
 __device__ __forceinline__ uint64_t vmajor_desc(uint32_t addr) { return smem_desc(addr, HALF_BYTES, 1024, 2); }
 
-// KV tiles a 64-token query tile needs: keys up to its last token's position.
-__device__ __forceinline__ int kv_tiles(int first_tok, int ql, int offset) {
+// KV tiles a query tile of qtok tokens needs: keys up to its last token's position.
+__device__ __forceinline__ int kv_tiles(int first_tok, int qtok, int ql, int offset) {
     if (first_tok >= ql) return 0;
-    const int last = min(first_tok + QTOK, ql) - 1;
+    const int last = min(first_tok + qtok, ql) - 1;
     return (last + offset + KT) / KT;     // ceil((last + offset + 1) / KT)
 }
 
@@ -171,8 +171,9 @@ __device__ __forceinline__ Unit unit_from(const Params& p, int idx, uint4 rec) {
     u.ql = static_cast<int>(rec.z);
     u.kl = static_cast<int>(rec.w);
     u.offset = u.kl - u.ql;
-    u.n[0] = kv_tiles(u.pair * UNIT_TOK, u.ql, u.offset);
-    u.n[1] = kv_tiles(u.pair * UNIT_TOK + QTOK, u.ql, u.offset);
+    const int qtok = ROWS >> p.lg;
+    u.n[0] = kv_tiles(u.pair * 2 * qtok, qtok, u.ql, u.offset);
+    u.n[1] = kv_tiles(u.pair * 2 * qtok + qtok, qtok, u.ql, u.offset);
     return u;
 }
 
@@ -202,16 +203,17 @@ static_assert(sizeof(RingEntry) == 32, "ring slots are 32 bytes");
 // tile, plus a little when B exists: measured per unit, a lone 8-tile A takes
 // 13.7 us against 8.7 us for 4 + 4 tiles.  The cost is therefore 2 max(nA, nB),
 // plus 1 when B exists (B never has fewer tiles than A).
-__device__ __forceinline__ int unit_cost(int pr, int ql, int off) {
-    const int na = kv_tiles(pr * UNIT_TOK, ql, off), nb = kv_tiles(pr * UNIT_TOK + QTOK, ql, off);
+__device__ __forceinline__ int unit_cost(int pr, int qtok, int ql, int off) {
+    const int na = kv_tiles(pr * 2 * qtok, qtok, ql, off), nb = kv_tiles(pr * 2 * qtok + qtok, qtok, ql, off);
     return 2 * max(na, nb) + (nb > 0 ? 1 : 0);
 }
 // -------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q,
                                                            const int32_t* __restrict__ cu_k, int num_seqs,
-                                                           int max_blocks, int block_size, int max_cost,
+                                                           int max_blocks, int block_size, int qtok, int max_cost,
                                                            uint4* __restrict__ plan, int* err) {
     extern __shared__ int hist[];          // [max_cost + 1]
+    const int unit_tok = 2 * qtok;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int i = threadIdx.x; i <= max_cost; i += blockDim.x) hist[i] = 0;
     __syncthreads();
@@ -227,8 +229,8 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
             continue;
         }
         const int off = kl - ql;
-        for (int pr = 0; pr * UNIT_TOK < ql; ++pr) {
-            const int cost = min(max_cost, unit_cost(pr, ql, off));
+        for (int pr = 0; pr * unit_tok < ql; ++pr) {
+            const int cost = min(max_cost, unit_cost(pr, qtok, ql, off));
             atomicAdd(&hist[cost], 1);
         }
     }
@@ -243,8 +245,8 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
         int ql, kl;
         if (!seq_ok(s, ql, kl)) continue;
         const int off = kl - ql;
-        for (int pr = 0; pr * UNIT_TOK < ql; ++pr) {
-            const int cost = min(max_cost, unit_cost(pr, ql, off));
+        for (int pr = 0; pr * unit_tok < ql; ++pr) {
+            const int cost = min(max_cost, unit_cost(pr, qtok, ql, off));
             const int pos = atomicAdd(&hist[cost], 1);
             plan[1 + pos] = make_uint4((static_cast<uint32_t>(s) << 16) | static_cast<uint32_t>(pr),
                                        static_cast<uint32_t>(cu_q[s]), static_cast<uint32_t>(ql),
@@ -362,13 +364,15 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const Unit u = unit_from(p, idx_cur, rec_cur);
                 const int n = max(u.n[0], u.n[1]);
                 if (uq >= 1 && !(ok = wait_phase(ctl, bar(BAR_QE), (uq - 1) & 1))) break;
-                const int qrow = u.q_start + u.pair * UNIT_TOK;
+                const int qtok = ROWS >> p.lg;
+                const int qrow = u.q_start + u.pair * 2 * qtok;
+                const int qhead = u.g << p.lg;
                 mbar_arrive_expect_tx(bar(BAR_QF), u.n[1] > 0 ? 2 * TILE_BYTES : TILE_BYTES);
-                tma_load_3d(sQ[0], &tm_q, bar(BAR_QF), 0, G * u.g, qrow);
-                tma_load_3d(sQ[0] + HALF_BYTES, &tm_q, bar(BAR_QF), 64, G * u.g, qrow);
+                tma_load_3d(sQ[0], &tm_q, bar(BAR_QF), 0, qhead, qrow);
+                tma_load_3d(sQ[0] + HALF_BYTES, &tm_q, bar(BAR_QF), 64, qhead, qrow);
                 if (u.n[1] > 0) {
-                    tma_load_3d(sQ[1], &tm_q, bar(BAR_QF), 0, G * u.g, qrow + QTOK);
-                    tma_load_3d(sQ[1] + HALF_BYTES, &tm_q, bar(BAR_QF), 64, G * u.g, qrow + QTOK);
+                    tma_load_3d(sQ[1], &tm_q, bar(BAR_QF), 0, qhead, qrow + qtok);
+                    tma_load_3d(sQ[1] + HALF_BYTES, &tm_q, bar(BAR_QF), 64, qhead, qrow + qtok);
                 }
                 ++uq;
                 for (int j = 0; j < n; ++j) {
@@ -538,7 +542,8 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ---------------------------------------------------------------- softmax, tile X
         const int X = warp >> 2;                  // 0: warps 0-3, 1: warps 4-7
         const int row = tid & 127;                // TMEM lane
-        const int ti = row >> 1;
+        const int ti = row >> p.lg;               // token of this row within the tile
+        const int qtok = ROWS >> p.lg;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_tmem = tmem + lane_off + S_COL(X);
         const uint32_t o_tmem = tmem + lane_off + O_COL(X);
@@ -557,7 +562,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const Unit u = unit_from(p, idx, rec);
             const int nx = X ? u.n[1] : u.n[0];
             if (nx == 0) continue;
-            const int qi = u.pair * UNIT_TOK + X * QTOK + ti;
+            const int qi = (2 * u.pair + X) * qtok + ti;
             const int jmax = min(qi + u.offset, u.kl - 1);
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < nx; ++j) {
@@ -670,10 +675,10 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const int k = lane & 7;
                     const uint4 w = ld_shared_v4(stg_s + rr * 128 + ((k ^ (rr & 7)) * 16));
                     const int lrow = (warp & 3) * 32 + rr;        // TMEM lane = tile row
-                    const int tok = u.pair * UNIT_TOK + X * QTOK + (lrow >> 1);
+                    const int tok = (2 * u.pair + X) * qtok + (lrow >> p.lg);
                     if (tok < u.ql) {
-                        uint16_t* d = p.out + (static_cast<int64_t>(u.q_start + tok) * p.num_heads + G * u.g +
-                                               (lrow & 1)) * D + 64 * half + 8 * k;
+                        uint16_t* d = p.out + (static_cast<int64_t>(u.q_start + tok) * p.num_heads + (u.g << p.lg) +
+                                               (lrow & ((1 << p.lg) - 1))) * D + 64 * half + 8 * k;
                         *reinterpret_cast<uint4*>(d) = w;
                     }
                 }
@@ -694,22 +699,26 @@ constexpr size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(25
 
 }  // namespace
 
-size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q) {
-    const size_t pairs = static_cast<size_t>(num_seqs) * ((max_seqlen_q + UNIT_TOK - 1) / UNIT_TOK);
+size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q, int log_group) {
+    const int unit_tok = 2 * (ROWS >> log_group);
+    const size_t pairs = static_cast<size_t>(num_seqs) * ((max_seqlen_q + unit_tok - 1) / unit_tok);
     return align256((pairs + 1) * 16);
 }
 
 pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     if (a.num_seqs == 0 || a.total_q == 0 || a.max_seqlen_q == 0) return PKV_OK;
-    if (a.max_seqlen_q > 0xffff * UNIT_TOK) return PKV_ERR_UNSUPPORTED;
-    const size_t need = prefill_workspace_bytes(a.num_seqs, a.max_seqlen_q);
+    const int lg = group_log2(a.num_heads, a.num_kv_heads);
+    if (lg < 0) return PKV_ERR_UNSUPPORTED;
+    const int qtok = ROWS >> lg, unit_tok = 2 * qtok;
+    if (a.max_seqlen_q > 0xffff * unit_tok) return PKV_ERR_UNSUPPORTED;
+    const size_t need = prefill_workspace_bytes(a.num_seqs, a.max_seqlen_q, lg);
     if (a.workspace == nullptr || a.workspace_bytes < need) return PKV_ERR_WORKSPACE;
     CUtensorMap tm_q, tm_k, tm_v;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_heads),
                                   static_cast<uint64_t>(a.total_q)};
         const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.num_heads) * D * 2};
-        const uint32_t box[3] = {64u, static_cast<uint32_t>(G), static_cast<uint32_t>(QTOK)};
+        const uint32_t box[3] = {64u, static_cast<uint32_t>(1 << lg), static_cast<uint32_t>(qtok)};
         if (encode_tiled(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(a.q), dims, strides,
                          box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return PKV_ERR_INVALID_ARG;
@@ -740,6 +749,7 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     p.max_blocks = a.max_blocks;
     p.num_heads = a.num_heads;
     p.num_kv_heads = a.num_kv_heads;
+    p.lg = lg;
     p.block_size = a.block_size;
     p.num_blocks = a.num_blocks;
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
@@ -759,11 +769,11 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     }();
     if (launch_regs < static_cast<int>(kMinLaunchRegs)) return PKV_ERR_UNSUPPORTED;
     prefill_plan_kernel<<<1, 1024, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.max_blocks, a.block_size,
-                                                        max_cost, static_cast<uint4*>(a.workspace), err);
+                                                        qtok, max_cost, static_cast<uint4*>(a.workspace), err);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
 
     const int64_t max_units = static_cast<int64_t>(a.num_seqs) *
-                              ((a.max_seqlen_q + UNIT_TOK - 1) / UNIT_TOK) * a.num_kv_heads;
+                              ((a.max_seqlen_q + unit_tok - 1) / unit_tok) * a.num_kv_heads;
     const int grid = static_cast<int>(std::min<int64_t>(sm_count(), max_units));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -55,10 +55,23 @@ def test_host_argument_checks_return_before_launch(lib):
     # store: negative token count; row stride smaller than a row
     assert lib.pkv_store_kvcache(P, P, -1, 1024, 1024, P, P, P, 4, 256, 8, 128, P) == 1
     assert lib.pkv_store_kvcache(P, P, 4, 512, 1024, P, P, P, 4, 256, 8, 128, P) == 1
-    # decode: unsupported head_dim / group / block size
+    # decode: unsupported head_dim / group (3 and 16 query heads per KV head) / block size
     assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 8, 64, 256, 4, 0.1, P, P, 0, P) == 2
-    assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 4, 128, 256, 4, 0.1, P, P, 0, P) == 2
+    assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 12, 4, 128, 256, 4, 0.1, P, P, 0, P) == 2
+    assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 1, 128, 256, 4, 0.1, P, P, 0, P) == 2
     assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 8, 128, 100, 4, 0.1, P, P, 0, P) == 2
+    # every supported group (1, 2, 4, 8) passes the shape check and stops at the null pointers
+    for hq, hkv in ((16, 16), (16, 8), (16, 4), (16, 2), (32, 4), (8, 1)):
+        assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, hq, hkv, 128, 256, 4, 0.1, P, P, 0, P) == 1
+        assert lib.pkv_prefill_varlen(P, P, P, P, P, P, 4, 2, 10, 9, 9, hq, hkv, 128, 256, 4, 0.1, P, P, 0, P) == 1
+        assert lib.pkv_prefill_workspace_size(4, hq, hkv, 128, 100) > 0
+    assert lib.pkv_prefill_varlen(P, P, P, P, P, P, 4, 2, 10, 9, 9, 12, 4, 128, 256, 4, 0.1, P, P, 0, P) == 2
+    assert lib.pkv_prefill_workspace_size(4, 12, 4, 128, 100) == 0
+    assert lib.pkv_decode_workspace_size(4, 12, 4, 128) == 0
+    # decode, decode_append: a softmax scale that is not a positive finite number
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        assert lib.pkv_decode(P, P, P, P, 4, P, 2, 10, 16, 8, 128, 256, 4, bad, P, P, 0, P) == 1
+        assert lib.pkv_decode_append(P, P, P, P, P, P, 4, P, 2, 10, 16, 8, 128, 256, 4, bad, P, P, P, 0, P) == 1
     # prefill: max_seqlen_q > max_seqlen_k
     assert lib.pkv_prefill_varlen(P, P, P, P, P, P, 4, 2, 10, 9, 8, 16, 8, 128, 256, 4, 0.1, P, P, 0, P) == 1
     # slot mapping: both or neither of cu_seqlens_k / context_lens

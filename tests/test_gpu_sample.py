@@ -11,27 +11,9 @@ import torch
 
 import workloads as W
 from oracle import sampler as sm
+from pkv_testutil import NEAR_TIE, check_sampler_ids as _check_ids
 
 pytestmark = pytest.mark.gpu
-
-NEAR_TIE = 1e-4
-
-
-def _check_ids(ids_gpu, logits, temps, seed, offset=0, max_near=2):
-    lg = logits.cpu().double().numpy()
-    T = temps.cpu().double().numpy()
-    e = sm.exponential_noise(seed, offset, range(lg.shape[0]), lg.shape[1])
-    ref, margin = sm.exponential_race(lg, T, e)
-    got = ids_gpu.cpu().numpy()
-    near = margin < NEAR_TIE
-    assert np.array_equal(got[~near], ref[~near]), np.nonzero(got[~near] != ref[~near])
-    for b in np.nonzero(near)[0]:
-        z = lg[b] / T[b]
-        r = np.exp(z - z.max()) / e[b]
-        top2 = np.argsort(r)[-2:]
-        assert got[b] in top2
-    assert near.sum() <= max_near
-    return int(near.sum())
 
 
 @pytest.mark.parametrize("vocab", [1000, 1001, 7])

@@ -1,5 +1,6 @@
 """Supported shapes beyond the benchmark's: block sizes that are other multiples of
-256 tokens, and other KV-head counts (two query heads per KV head), through the
+256 tokens, other KV-head counts, and every supported group size (query heads per
+KV head: MHA 1, GQA 2, 4 and 8; atlas fig. 18 draws MHA, GQA and MQA), through the
 slot mapping, the scatter, prefill, decode and the fused decode, against the
 fp64 oracle.  Lengths are chosen to sit on and next to block edges."""
 import numpy as np
@@ -17,6 +18,11 @@ SHAPES = {
     "heads4-2": dict(num_heads=4, num_kv_heads=2),
     "heads8-4": dict(num_heads=8, num_kv_heads=4),
     "heads32-16": dict(num_heads=32, num_kv_heads=16),
+    "mha16-16": dict(num_heads=16, num_kv_heads=16),
+    "gqa16-4": dict(num_heads=16, num_kv_heads=4),
+    "gqa16-2": dict(num_heads=16, num_kv_heads=2),
+    "gqa32-4": dict(num_heads=32, num_kv_heads=4),
+    "mqa8-1": dict(num_heads=8, num_kv_heads=1),
 }
 
 # prefill: whole prompts, chunks after a prefix that ends mid-block, single-token chunks
