@@ -170,6 +170,11 @@ class _on_device:
         return False
 
 
+def _row_stride(logits: torch.Tensor) -> int:
+    """Elements between rows; a single row's stride is meaningless (it may be 0), so use its length."""
+    return logits.stride(0) if logits.shape[0] > 1 else logits.shape[1]
+
+
 def _raise(status: int, where: str):
     if status != 0:
         raise PkvError(status, where)
@@ -462,7 +467,7 @@ def pkv_sample(logits: torch.Tensor, temperatures: torch.Tensor, seed: int, offs
         out_ids = torch.empty(batch, dtype=torch.int64, device=logits.device)
     _check(out_ids, "out_ids", torch.int64, 1)
     with _on_device(logits, temperatures, out_ids, stream=stream):
-        _raise(load().pkv_sample(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures),
+        _raise(load().pkv_sample(_ptr(logits), batch, vocab, _row_stride(logits), _ptr(temperatures),
                                  int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), _ptr(out_ids),
                                  _stream(stream)), "pkv_sample")
     return out_ids
@@ -484,7 +489,8 @@ def pkv_sample_dev(logits: torch.Tensor, temperatures: torch.Tensor, seed_offset
         out_ids = torch.empty(batch, dtype=torch.int64, device=logits.device)
     _check(out_ids, "out_ids", torch.int64, 1)
     with _on_device(logits, temperatures, seed_offset, out_ids, stream=stream):
-        _raise(load().pkv_sample_dev(_ptr(logits), batch, vocab, logits.stride(0), _ptr(temperatures), _ptr(seed_offset),
+        _raise(load().pkv_sample_dev(_ptr(logits), batch, vocab, _row_stride(logits), _ptr(temperatures),
+                                     _ptr(seed_offset),
                                      _ptr(out_ids), _stream(stream)), "pkv_sample_dev")
     return out_ids
 

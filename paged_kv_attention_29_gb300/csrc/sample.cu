@@ -92,10 +92,22 @@ __device__ __forceinline__ bool better(float k, int i, float bk, int bi) {
 }
 
 __device__ __forceinline__ void consider(float logit, float inv_t, uint32_t x, int col, float& bk, int& bi) {
-    const float u = __uint2float_rn(2u * (x >> 9) + 1u) * 5.9604644775390625e-08f;   // 2^-24
-    // hardware log2 (absolute error ~1e-7 in ln): the key is decided to ~1e-6, far below the
-    // spacing at which two candidates could swap
-    const float e = -__logf(u);
+    // e = -ln u.  Near u = 1, where e is tiny and the key large, e must come from the exact
+    // w = 1 - u (u = 1 - k 2^-24 gives e ~ k 2^-24, far below the absolute error of a fast
+    // logarithm of u itself, which then mis-ranks exactly the elements most likely to win):
+    // for w < 2^-6, e = -ln(1 - w) = w + w^2/2 + w^3/3 + w^4/4 + ..., the dropped terms
+    // below 2^-24 of e.  Elsewhere |ln u| > 2^-6 and the hardware log2 (absolute error about
+    // 1e-7) gives e to better than 1e-5 relative; the key -ln e then has an absolute error
+    // below 1e-5, well inside the spacing at which two candidates could swap.
+    const uint32_t m = x >> 9;
+    const float w = __uint2float_rn(2u * (0x7fffffu - m) + 1u) * 5.9604644775390625e-08f;   // 1 - u, exact
+    float e;
+    if (w < 0.015625f) {
+        e = w * fmaf(w, fmaf(w, fmaf(w, 0.25f, 0.333333343f), 0.5f), 1.0f);
+    } else {
+        const float u = __uint2float_rn(2u * m + 1u) * 5.9604644775390625e-08f;               // 2^-24
+        e = -__logf(u);
+    }
     const float key = logit * inv_t - __logf(e);
     // NaN keys never win; a -inf key only wins against nothing and is rejected
     if (key == key && key > -INFINITY && better(key, col, bk, bi)) {

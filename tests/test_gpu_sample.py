@@ -25,10 +25,47 @@ def test_sample_small_vs_oracle(pkv, vocab):
     assert code == 0
 
 
-def test_sample_full_vocab_vs_oracle(pkv):
-    s = W.sampler_inputs(batch=256, vocab=W.VOCAB_QWEN3, seed=1005, step=0, device="cpu")
+@pytest.mark.parametrize("step", [0, 1, 3])
+def test_sample_full_vocab_vs_oracle(pkv, step):
+    """The full decode step's sampler, [256, 151936] logits, with the noise of several steps
+    (steps 1 and 3 each held rows whose winner's noise u sits within a few 2^-24 of 1)."""
+    s = W.sampler_inputs(batch=256, vocab=W.VOCAB_QWEN3, seed=1005, step=step, device="cpu")
     ids = pkv.pkv_sample(s.logits.cuda(), s.temperatures.cuda(), s.seed, s.offset)
     _check_ids(ids, s.logits, s.temperatures, s.seed, s.offset)
+
+
+def test_sample_noise_next_to_one_is_ranked_exactly(pkv):
+    """An element whose noise u lies within a few 2^-24 of 1 has a tiny e = -ln u and so a key
+    about 16 above its scaled logit: the elements most likely to win.  Its key must come out
+    exact.  The oracle's generator finds such an element; its row is rebuilt so that this
+    element's exact key sits 0.3 below, then 0.3 above, one competitor in another slice of
+    the row (every other logit far below), and the ids must follow the oracle both times."""
+    V, seed = W.VOCAB_QWEN3, 9001
+    found = None
+    for r0 in range(0, 512, 32):
+        x = sm.noise_bits(seed, 0, range(r0, r0 + 32), V) >> np.uint32(9)
+        hits = np.argwhere(x >= np.uint32((1 << 23) - 4))
+        if len(hits):
+            found = (r0 + int(hits[0][0]), int(hits[0][1]))
+            break
+    assert found is not None
+    row, v = found
+    c = (v + V // 2) % V                                   # a competitor in another eighth of the row
+    e = sm.exponential_noise(seed, row, [0], V)[0]          # the noise of that row (offset = row)
+    assert e[v] < 1e-6
+    for delta in (-0.3, 0.3):
+        lg = np.full(V, -60.0)
+        lg[c] = 0.0
+        key_c = lg[c] + np.log(1.0 / e[c])
+        lg[v] = key_c + delta + np.log(e[v])                 # exact key of v = key_c + delta
+        logits = torch.tensor(lg, dtype=torch.float32).reshape(1, V)
+        temps = torch.ones(1)
+        ids = pkv.pkv_sample(logits.cuda(), temps.cuda(), seed, offset=row)
+        ref, margin = sm.exponential_race(logits.double().numpy(), temps.double().numpy(), e[None, :])
+        assert margin[0] > 0.1
+        assert int(ids.item()) == int(ref[0]) == (v if delta > 0 else c)
+    code, _ = pkv.pkv_get_device_error(clear=True)
+    assert code == 0
 
 
 def test_sample_row_offset_and_strided_rows(pkv):
