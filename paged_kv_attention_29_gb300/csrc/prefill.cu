@@ -23,6 +23,10 @@
 // no further wait; O is rescaled only when a row max grows by more than 2^8
 // (P then stays below 256, and O and the row sum share the stale max).
 //
+// The softmax warps' code is kept small: two softmax warps share each
+// scheduler, and rolling the rare rescale loop and the epilogue's outer loop
+// (no spills left) took a call from 54.9 to 51.9 us, bit-identical.
+//
 // The softmax is the critical path, so it is written for the fewest issued
 // instructions per score: one 3-input max per two scores, the exponent
 // argument as one packed fp32x2 FMA per two scores, one special-function
@@ -599,7 +603,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     // S_X(j) landed, so PV_X(j-1) has too: O_X is stable until P_X(j) is released
                     const float m_tgt = fmaxf(m_used, m_new);
                     const float alpha = ex2_ftz(m_used - m_tgt);
-#pragma unroll
+#pragma unroll 1     // a rare path, kept rolled: its registers and code stay out of the hot loop
                     for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
                         tmem_ld32(o_tmem + 32 * c, o);
@@ -650,7 +654,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const float inv = 1.f / l;
             uint8_t* stg = gbase + SM_STAGE + warp * STAGE_WARP_BYTES;
             const uint32_t stg_s = smem_u32(stg);
-#pragma unroll
+#pragma unroll 1     // kept rolled: the softmax warps' code must stay small (see below)
             for (int half = 0; half < 2; ++half) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
