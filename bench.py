@@ -713,6 +713,31 @@ def bench_decode_sweep(args, pkv, torch, peaks):
                         "L2 flushed before every call (median of 20)", "rows": rows}
 
 
+def bench_sample(args, pkv, torch, peaks):
+    """The sampler alone on the full decode step's logits ([256, 151936] fp32), L2 flushed before
+    each call (the logits, 156 MB, are larger than L2 anyway)."""
+    s_in = W.sampler_inputs(batch=256, device="cuda")
+    ids = torch.empty(256, dtype=torch.int64, device="cuda")
+    flush = L2Flush(torch)
+    for k in range(3):
+        pkv.pkv_sample(s_in.logits, s_in.temperatures, s_in.seed + k, 0, out_ids=ids)
+    ms = []
+    for k in range(max(10, min(100, args.steps // 30))):
+        flush_l2(torch, flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pkv.pkv_sample(s_in.logits, s_in.temperatures, s_in.seed + k, 0, out_ids=ids)
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    call = float(np.median(ms))
+    nbytes = 256 * W.VOCAB_QWEN3 * 4
+    gbs = nbytes / (call * 1e-3) / 1e9
+    return {"workload": "temperature sampler on [256, 151936] fp32 logits N(0, 3^2), T in [0.5, 1]",
+            "gbs": gbs, "unit": "GB/s", "call_ms_median": call, "frac_of_hbm": gbs / peaks[0],
+            "algorithmic_bytes": nbytes, "l2": "flushed before every call"}
+
+
 def bench_full_step(args, pkv, torch, peaks):
     wl = W.full_step()
     st = DecodeStep(pkv, torch, wl, layers=wl.num_layers)
@@ -798,8 +823,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--no-secondary", action="store_true", help="headline only")
-    ap.add_argument("--parts", default="prefill,long,full,rope",
-                    help="secondary workloads to run: any of prefill,long,full,rope,sweep (sweep is opt-in)")
+    ap.add_argument("--parts", default="prefill,long,full,rope,sample",
+                    help="secondary workloads to run: any of prefill,long,full,rope,sample,sweep (sweep is opt-in)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     args = ap.parse_args(argv)
@@ -831,7 +856,7 @@ def main(argv=None):
         # (ncu --nvtx --nvtx-include "full_step/")
         for key, part, fn in (("prefill", "prefill", bench_prefill), ("long", "long_decode", bench_long_decode),
                               ("full", "full_step", bench_full_step), ("rope", "rope_store", bench_rope_store),
-                              ("sweep", "decode_sweep", bench_decode_sweep)):
+                              ("sample", "sample", bench_sample), ("sweep", "decode_sweep", bench_decode_sweep)):
             if key in parts:
                 torch.cuda.nvtx.range_push(part)
                 try:
