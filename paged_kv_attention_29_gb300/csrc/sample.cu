@@ -84,6 +84,16 @@ __device__ __forceinline__ uint4 philox_row_at(uint32_t q, const PhiloxRow& r, c
     return c;
 }
 
+// 1 - u of a noise word, exactly: with m = x >> 9, f = 1 + (2^23 - 1 - m) 2^-23 in [1, 2) has the
+// complemented mantissa bits, and 1 - u = (2^24 - 2m - 1) 2^-24 = f - (1 - 2^-24), a difference
+// of two floats within a factor of two of each other and therefore exact.
+// ex2.approx, which the candidate bounds use, is within 2^-22 relatively, well inside their
+// 1.001 margin; a bound flushed to zero only skips elements that cannot win (1 - u >= 2^-24).
+__device__ __forceinline__ float one_minus_u_of(uint32_t x) {
+    const float f = __uint_as_float(0x3F800000u | (~x >> 9));
+    return f - 0.999999940395355224609375f;
+}
+
 // (key, index) with "better" = larger key, then lower index; index < 0 = none.
 __device__ __forceinline__ bool better(float k, int i, float bk, int bi) {
     if (i < 0) return false;
@@ -118,8 +128,10 @@ __device__ __forceinline__ void consider(float logit, float inv_t, uint32_t x, i
 
 // kParamKeys: the seed came from the host and `rk` holds its round keys; otherwise the
 // seed and row offset are read from `seed_offset` and the keys computed here.
+// The loop is bound by instruction issue, so the kernel is held to 32 registers: eight
+// CTAs (64 warps) resident per SM.
 template <bool kParamKeys>
-__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS)
+__global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS, 8)
 sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stride,
                    const float* __restrict__ temperatures, uint32_t key0, uint32_t key1,
                    uint64_t offset, const uint64_t* __restrict__ seed_offset, int vec_ok,
@@ -162,11 +174,12 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
         // (u <= 1 - 2^-24), so a quad whose largest l/T + 16.7 is below `best` has
         // no candidate at all and skips its Philox call.  `best` is the warp's
         // running maximum; t carries a 1e-3 margin and the bound a factor 1.001,
-        // so rounding and exact ties are always decided by the exact key.  Within
-        // a quad that does draw noise, the per-element test has no branch; only a
-        // quad with a candidate branches to the exact key.  Skipped elements
-        // cannot change the winner: some element of the warp already has a
-        // larger key.
+        // so rounding and exact ties are always decided by the exact key.  A quad
+        // that does draw noise is first tested as a whole: its smallest 1 - u (its
+        // largest word) against the bound of its largest logit.  Any candidate
+        // passes that test, and only a passing quad tests its elements one by one
+        // and takes the exact key of each candidate.  Skipped elements cannot
+        // change the winner: some element of the warp already has a larger key.
         const int iters = (q1 - q0 + THREADS - 1) / THREADS;     // uniform across the CTA
         float wbest = -INFINITY;
         // the next quad's logits are loaded one iteration ahead, so the load is in flight while
@@ -181,42 +194,51 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
                 for (int e = 0; e < 4; ++e) l[e] = (qd < q1 && col + e < vocab) ? __ldcs(lrow + col + e) : -INFINITY;
             }
         };
-        float ln[4];
-        load_quad(q0 + tid, ln);
-        for (int it = 0; it < iters; ++it) {
-            const int qd = q0 + it * THREADS + tid;
-            float l[4] = {ln[0], ln[1], ln[2], ln[3]};
-            if (it + 1 < iters) load_quad(qd + THREADS, ln);
-            if (qd < q1) {
-                const int col = qd * 4;
-                const float best = fmaxf(bk, wbest);
-                const float lmax = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
-                // (NaN logits fail this test; their bound below is NaN, so they are never candidates)
-                if (!(lmax * inv_t + 16.7f < best)) {
-                    const uint4 x = philox_row_at<kParamKeys>(static_cast<uint32_t>(qd), prow, rk);
+        auto examine = [&](int qd, const float (&l)[4]) {
+            const int col = qd * 4;
+            const float best = wbest;     // the warp's best after the previous quad, so never below bk
+            const float lmax = fmax3(l[0], l[1], fmaxf(l[2], l[3]));
+            // (NaN logits fail this test; their bound below is NaN, so they are never candidates)
+            if (!(lmax * inv_t + 16.7f < best)) {
+                const uint4 x = philox_row_at<kParamKeys>(static_cast<uint32_t>(qd), prow, rk);
+                // candidate test: 1 - u < 1.001 e^-t, t = best - l/T - 1e-3, as 1 - u < 2^(l (log2 e / T) + cb).
+                // t <= 0 gives a bound above 1 (always a candidate); l = -inf (padding past the
+                // vocabulary) gives 0 (never); NaN never.
+                const float cb = (1e-3f - best) * 1.4426950408889634f + 1.4419741739064e-3f;   // + log2 1.001
+                const uint32_t xmax = max(max(x.x, x.y), max(x.z, x.w));
+                if (one_minus_u_of(xmax) < ex2_ftz(fmaf(lmax, inv_t_log2e, cb))) {
                     const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-                    // candidate test, branch-free: 1 - u < 1.001 e^-t, t = best - l/T - 1e-3, as
-                    // 1 - u < 2^(l (log2 e / T) + cb).  t <= 0 gives a bound above 1 (always a
-                    // candidate); l = -inf (padding past the vocabulary) gives 0 (never); NaN never.
-                    const float cb = (1e-3f - best) * 1.4426950408889634f + 1.4419741739064e-3f;   // + log2 1.001
-                    bool cand[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // 1 - u exactly: f = 1 + (x >> 9) 2^-23 in [1, 2), 1 - u = (2 - f) - 2^-24
-                        const float f = __uint_as_float(0x3F800000u | (xs[e] >> 9));
-                        const float one_minus_u = (2.0f - f) - 5.9604644775390625e-08f;
-                        // ex2.approx is within 2^-22 relatively, well inside the 1.001 margin; a
-                        // bound flushed to zero only skips elements that cannot win (1 - u >= 2^-24)
-                        cand[e] = one_minus_u < ex2_ftz(fmaf(l[e], inv_t_log2e, cb));
-                    }
-                    if (cand[0] | cand[1] | cand[2] | cand[3]) {   // rare once `best` has settled
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (cand[e]) consider(l[e], inv_t, xs[e], col + e, bk, bi);
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        if (one_minus_u_of(xs[e]) < ex2_ftz(fmaf(l[e], inv_t_log2e, cb)))
+                            consider(l[e], inv_t, xs[e], col + e, bk, bi);
                 }
             }
+        };
+        // iterations in which every thread's quad exists and is four aligned columns: no checks
+        const int q1_whole = (vocab & 3) ? min(q1, nquads - 1) : q1;
+        const int nbulk = vec_ok ? max(0, (q1_whole - q0) / THREADS) : 0;
+        float ln[4];
+        load_quad(q0 + tid, ln);
+        int it = 0;
+        for (; it < nbulk; ++it) {
+            const int qd = q0 + it * THREADS + tid;
+            const float l[4] = {ln[0], ln[1], ln[2], ln[3]};
+            if (it + 1 < nbulk) {
+                const float4 l4 = __ldcs(reinterpret_cast<const float4*>(lrow + (qd + THREADS) * 4));
+                ln[0] = l4.x; ln[1] = l4.y; ln[2] = l4.z; ln[3] = l4.w;
+            } else if (it + 1 < iters) {
+                load_quad(qd + THREADS, ln);
+            }
+            examine(qd, l);
             // share the running best across the warp (NaN never enters a key)
+            asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wbest) : "f"(bk));
+        }
+        for (; it < iters; ++it) {
+            const int qd = q0 + it * THREADS + tid;
+            const float l[4] = {ln[0], ln[1], ln[2], ln[3]};
+            if (it + 1 < iters) load_quad(qd + THREADS, ln);
+            if (qd < q1) examine(qd, l);
             asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(wbest) : "f"(bk));
         }
     } else if (rank == 0 && tid == 0) {
