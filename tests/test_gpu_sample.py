@@ -77,6 +77,18 @@ def test_sample_row_offset_and_strided_rows(pkv):
     _check_ids(ids, s.logits, s.temperatures, 77, 1000)
 
 
+def test_sample_rows_not_16_byte_aligned(pkv):
+    """Rows that start off a 16-byte boundary (a view one column in, row stride 3002 floats)
+    take the scalar-load path for every quad; ids must not change."""
+    s = W.sampler_inputs(batch=16, vocab=3000, seed=33, device="cpu")
+    wide = torch.zeros(16, 3002)
+    wide[:, 1:3001] = s.logits
+    view = wide.cuda()[:, 1:3001]
+    assert view.data_ptr() % 16 != 0 and view.stride(0) % 4 != 0
+    ids = pkv.pkv_sample(view, s.temperatures.cuda(), s.seed, s.offset)
+    _check_ids(ids, s.logits, s.temperatures, s.seed, s.offset)
+
+
 def test_sample_cold_temperature_is_argmax(pkv):
     g = torch.Generator().manual_seed(33)
     logits = torch.randn(64, 512, generator=g) * 3
