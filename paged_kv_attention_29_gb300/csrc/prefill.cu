@@ -35,8 +35,10 @@
 //
 // Persistent CTAs (one per SM) take units from a list that a one-CTA plan
 // kernel sorts by cost (the longer tile's KV tiles, costliest first) and leaves
-// in the workspace: each CTA's producer claims the next unit with an atomic
-// increment when its current unit starts.  The two launches are chained with
+// in the workspace: CTA i starts with unit i, and each CTA's producer claims
+// its next unit with an atomic increment when its current unit starts.  The
+// plan's scan over cost buckets runs on a warp, 32 buckets per step.  The two
+// launches are chained with
 // programmatic dependent launch so this kernel's set-up overlaps the plan.
 //
 // Warps 0-3: softmax of tile A (TMEM lanes 0-127), warps 4-7: tile B; warp 8:
@@ -96,7 +98,7 @@ struct Params {
     const int32_t* block_tables;
     const uint4* plan;        // [0].x = number of (seq, pair) records, [0].y = unit counter;
                               // then {seq << 16 | pair, q_start, q_len, k_len}, costliest first
-    unsigned int* next_unit;  // &plan[0].y: units are taken in list order by atomic increments
+    unsigned int* next_unit;  // &plan[0].y: units from gridDim.x on are taken in list order by atomic increments
     uint16_t* out;
     int max_blocks;
     int num_heads;
@@ -181,11 +183,11 @@ __device__ __forceinline__ Unit unit_from(const Params& p, int idx, uint4 rec) {
     return u;
 }
 
-// Next unit of the cost-sorted list for this CTA, or -1: CTAs take units in
-// list order as they free up (longest first, so the last units to start are
-// the shortest and the CTAs finish close together).
+// Next unit of the cost-sorted list for this CTA, or -1: CTA i starts with unit i,
+// and after that CTAs take units in list order as they free up (longest first,
+// so the last units to start are the shortest and the CTAs finish close together).
 __device__ __forceinline__ int grab_unit(const Params& p, int total) {
-    const int idx = static_cast<int>(atomicAdd(p.next_unit, 1u));
+    const int idx = static_cast<int>(atomicAdd(p.next_unit, 1u) + gridDim.x);
     return idx < total ? idx : -1;
 }
 
@@ -212,7 +214,7 @@ __device__ __forceinline__ int unit_cost(int pr, int qtok, int ql, int off) {
     return 2 * max(na, nb) + (nb > 0 ? 1 : 0);
 }
 // -------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __restrict__ cu_q,
+__global__ void __launch_bounds__(256) prefill_plan_kernel(const int32_t* __restrict__ cu_q,
                                                            const int32_t* __restrict__ cu_k, int num_seqs,
                                                            int max_blocks, int block_size, int qtok, int max_cost,
                                                            uint4* __restrict__ plan, int* err) {
@@ -239,10 +241,23 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* __res
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    // exclusive scan in descending cost order (costliest first), 32 buckets per step of warp 0
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
         int run = 0;
-        for (int c = max_cost; c >= 0; --c) { const int x = hist[c]; hist[c] = run; run += x; }
-        plan[0] = make_uint4(static_cast<uint32_t>(run), 0u, 0u, 0u);
+        for (int top = max_cost; top >= 0; top -= 32) {
+            const int c = top - lane;
+            const int x = c >= 0 ? hist[c] : 0;
+            int incl = x;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            if (c >= 0) hist[c] = run + incl - x;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) plan[0] = make_uint4(static_cast<uint32_t>(run), 0u, 0u, 0u);
     }
     __syncthreads();
     for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
@@ -344,8 +359,9 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             int pref_idx = -2, pref_tile = -1;        // what `pref` locates
             // one unit of lookahead: the next unit is taken when the current one starts (its first K
             // tile rides in the current unit's last group), so no CTA holds more than one unit it
-            // has not started
-            int idx_cur = grab_unit(p, total_units);
+            // has not started.  The first unit of CTA i is unit i (no atomic round trip before the
+            // first copies); the queue hands out the rest from unit gridDim.x on.
+            int idx_cur = static_cast<int>(blockIdx.x) < total_units ? static_cast<int>(blockIdx.x) : -1;
             uint4 rec_cur = unit_record(p, idx_cur);
             bool ok = true;
             if (idx_cur >= 0) {                       // group 0: the first unit's first K tile
@@ -772,7 +788,7 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
         return cudaFuncGetAttributes(&fa, prefill_fa_kernel) == cudaSuccess ? fa.numRegs : -1;
     }();
     if (launch_regs < static_cast<int>(kMinLaunchRegs)) return PKV_ERR_UNSUPPORTED;
-    prefill_plan_kernel<<<1, 1024, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.max_blocks, a.block_size,
+    prefill_plan_kernel<<<1, 256, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.max_blocks, a.block_size,
                                                         qtok, max_cost, static_cast<uint4*>(a.workspace), err);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
 
