@@ -572,15 +572,38 @@ def bench_prefill(args, pkv, torch, peaks):
         torch.cuda.synchronize()
         step_ms.append(s.elapsed_time(e))
         call_ms.append(a.elapsed_time(b))
+    # the same attention on a plan made once for the batch (as every layer after the first of a
+    # model's prefill step runs): pkv_prefill_plan before the loop, pkv_prefill_varlen_planned timed
+    ws = pkv.pkv_prefill_plan(cu_q, cu_k, wl.total_q, int(wl.q_lens.max()), int(wl.kv_lens.max()), wl.num_heads,
+                              wl.num_kv_heads, wl.head_dim, wl.block_size, bt.shape[1])
+    planned_ms = []
+    for i in range(K + 3):
+        pkv.pkv_slot_mapping(bt, wl.num_blocks, wl.block_size, slots, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
+        pkv.pkv_store_kvcache(v.k_new, v.v_new, slots, v.k_cache, v.v_cache)
+        flush_l2(torch, flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        pkv.pkv_prefill_varlen_planned(v.q, v.k_cache, v.v_cache, cu_q, cu_k, bt, int(wl.q_lens.max()),
+                                       int(wl.kv_lens.max()), wl.softmax_scale, ws, out=out)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            planned_ms.append(a.elapsed_time(b))
     _, bf16, bf16_sus, kind = peaks
     call = float(np.median(call_ms))
     tflops = flops / (call * 1e-3) / 1e12
+    pcall = float(np.median(planned_ms))
+    ptflops = flops / (pcall * 1e-3) / 1e12
     return {"workload": "varlen prefill with prefix-cache hits: 32 prompts U[100,1024], 0-2 shared 256-token blocks "
                         "per group of 4, Hq 16, Hkv 8, d 128, bf16",
             "tflops": tflops, "unit": "TFLOP/s", "algorithmic_flops": int(flops), "call_ms_median": call,
             "step_ms_median": float(np.median(step_ms)), "frac_of_bf16_peak": tflops / bf16,
             "peak": bf16, "peak_source": kind, "steps": K, "l2": "flushed between steps (256 MB write, then 256 MB clean read)",
-            "total_q": wl.total_q}
+            "total_q": wl.total_q,
+            "planned": {"tflops": ptflops, "call_ms_median": pcall, "frac_of_bf16_peak": ptflops / bf16,
+                        "steps": K, "how": "pkv_prefill_plan once for the batch, then pkv_prefill_varlen_planned per "
+                                           "call (each layer after the first of a prefill step); L2 flushed before "
+                                           "each call"}}
 
 
 def bench_rope_store(args, pkv, torch, peaks):

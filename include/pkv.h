@@ -74,7 +74,8 @@ enum {
     PKV_DEVERR_SEQLENS = 3,      /* cu_seqlens decreasing, q_len > k_len, or a length above its max_* bound */
     PKV_DEVERR_TEMPERATURE = 4,  /* temperature <= 0, inf or NaN */
     PKV_DEVERR_TIMEOUT = 5,      /* an mbarrier wait exceeded its limit */
-    PKV_DEVERR_BLOCK_TABLE = 6   /* a position past max_blocks_per_seq * block_size */
+    PKV_DEVERR_BLOCK_TABLE = 6,  /* a position past max_blocks_per_seq * block_size */
+    PKV_DEVERR_PLAN = 7          /* the prefill workspace holds no plan for these arguments */
 };
 
 /* ABI version; bumped on any signature change. */
@@ -181,9 +182,11 @@ PKV_API pkv_status pkv_rope_store_kvcache(const pkv_bf16 *q, int64_t q_token_str
  *   max_seqlen_q / max_seqlen_k  bounds on q_len / k_len (host-known)
  *   softmax_scale  > 0
  *   workspace  >= pkv_prefill_workspace_size(num_seqs, num_heads, num_kv_heads,
- *        head_dim, max_seqlen_q) bytes: the work list, sorted by cost, that a
- *        planning launch writes before the attention launch reads it; needs no
- *        initialisation
+ *        head_dim, max_seqlen_q) bytes, 16-byte aligned: the work list, sorted
+ *        by cost, that a planning launch writes before the attention launch
+ *        reads it; needs no initialisation.  A sequence whose query rows fall
+ *        outside [0, total_q), or whose lengths break the bounds above, is left
+ *        out of the list and PKV_DEVERR_SEQLENS recorded.
  * Accumulation in fp32, probabilities rounded to bf16 for the PV product,
  * output rounded to bf16 once.
  */
@@ -198,6 +201,45 @@ PKV_API pkv_status pkv_prefill_varlen(const pkv_bf16 *q, const pkv_bf16 *k_cache
                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
                               float softmax_scale, pkv_bf16 *out, void *workspace,
                               size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * a3, planned once per batch.  The engine prepares a step's inputs (cu_seqlens,
+ * block tables) once, before the model runs (Nano-vLLM overview, the component
+ * table: the model runner's prepare_prefill, then run), and every layer's
+ * attention reads the same ones, so the work list can be made once and used by
+ * every layer:
+ *
+ *   pkv_prefill_plan     writes the cost-sorted work list into workspace (one
+ *                        small launch); it reads only cu_seqlens_q/k.
+ *   pkv_prefill_varlen_planned
+ *                        the attention of pkv_prefill_varlen, same arguments
+ *                        and result, without the planning launch.
+ *
+ * A planned call must get the num_seqs, total_q, max_seqlen_k, group size
+ * (num_heads / num_kv_heads), max_blocks_per_seq and block_size the plan was
+ * made with, and cu_seqlens_q/k must hold the same values.  The plan carries a
+ * tag of those arguments; a call whose arguments do not match it computes
+ * nothing and records PKV_DEVERR_PLAN.  Each call leaves the workspace ready for
+ * the next one, so any number of calls (each layer's pools, q and out) may
+ * follow one plan, in order on one stream; two calls on one workspace must not
+ * run at the same time.  A plan is valid until the workspace is reused for
+ * anything else; pkv_prefill_varlen also leaves a plan for its own arguments.
+ * Errors as for pkv_prefill_varlen (the plan checks only the arguments it takes).
+ */
+PKV_API pkv_status pkv_prefill_plan(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q,
+                            int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void *workspace,
+                            size_t workspace_bytes, pkv_stream_t stream);
+
+PKV_API pkv_status pkv_prefill_varlen_planned(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                                      const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                      int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                                      int32_t max_seqlen_k, int32_t num_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                      float softmax_scale, pkv_bf16 *out, void *workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream);
 
 /*
  * a4. Decode attention: one query token per sequence over its whole context.

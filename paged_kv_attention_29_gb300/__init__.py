@@ -28,7 +28,8 @@ import torch
 
 __all__ = [
     "PkvError", "load", "lib_path", "pkv_abi_version", "pkv_status_string", "pkv_slot_mapping",
-    "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen",
+    "pkv_store_kvcache", "pkv_prefill_workspace_size", "pkv_prefill_varlen", "pkv_prefill_plan",
+    "pkv_prefill_varlen_planned",
     "pkv_decode_workspace_size", "pkv_decode", "pkv_sample", "pkv_get_device_error", "pkv_check_wait_timeout",
     "WAIT_CHECK_INFO",
     "decode_workspace", "pkv_decode_append", "pkv_decode_noalloc", "pkv_sample_dev", "pkv_rope_store_kvcache", "DecodeAppendCall", "DEVERR",
@@ -39,7 +40,8 @@ _LIB_PATH = os.path.join(_HERE, "libpkv.so")
 _lib: Optional[ctypes.CDLL] = None
 
 DEVERR = {0: "none", 1: "block id outside pool", 2: "slot outside pool", 3: "sequence lengths",
-          4: "temperature", 5: "pipeline wait timed out", 6: "position past block table"}
+          4: "temperature", 5: "pipeline wait timed out", 6: "position past block table",
+          7: "no prefill plan for these arguments in the workspace"}
 
 _c_int32 = ctypes.c_int32
 _c_int64 = ctypes.c_int64
@@ -82,6 +84,12 @@ def load() -> ctypes.CDLL:
         "pkv_prefill_varlen": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_int32,
                                               _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
                                               _c_int32, _c_int32, _c_float, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+        "pkv_prefill_plan": (ctypes.c_int, [_c_ptr, _c_ptr, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
+                                            _c_int32, _c_int32, _c_int32, _c_int32, _c_ptr, _c_size, _c_ptr]),
+        "pkv_prefill_varlen_planned": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32,
+                                                      _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_int32,
+                                                      _c_int32, _c_int32, _c_int32, _c_float, _c_ptr, _c_ptr,
+                                                      _c_size, _c_ptr]),
         "pkv_decode_workspace_size": (_c_size, [_c_int32] * 4),
         "pkv_decode": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int32, _c_ptr, _c_int32, _c_int32,
                                       _c_int32, _c_int32, _c_int32, _c_int32, _c_int32, _c_float, _c_ptr,
@@ -285,11 +293,8 @@ def pkv_prefill_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int,
     return int(load().pkv_prefill_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_seqlen_q))
 
 
-def pkv_prefill_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cu_seqlens_q: torch.Tensor,
-                       cu_seqlens_k: torch.Tensor, block_tables: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
-                       softmax_scale: float, out: Optional[torch.Tensor] = None,
-                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Varlen prefill attention over the paged cache (the new tokens' K/V already stored)."""
+def _prefill(entry: str, q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, max_seqlen_q, max_seqlen_k,
+             softmax_scale, out, workspace, stream):
     nb, bs, hkv, d = _pool_shape(k_cache)
     _check(v_cache, "v_cache", torch.bfloat16, 4)
     _check(q, "q", torch.bfloat16, 3)
@@ -306,15 +311,58 @@ def pkv_prefill_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
         out = torch.empty_like(q)
     _check(out, "out", torch.bfloat16, 3)
     if workspace is None:
+        if entry == "pkv_prefill_varlen_planned":
+            raise ValueError("a planned prefill needs the workspace its plan was written to")
         n = pkv_prefill_workspace_size(num_seqs, hq, hkv, d, int(max_seqlen_q))
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     with _on_device(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, out, workspace, stream=stream):
-        _raise(load().pkv_prefill_varlen(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                                         _ptr(block_tables), block_tables.shape[1], num_seqs, total_q, int(max_seqlen_q),
-                                         int(max_seqlen_k), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
-                                         _ptr(workspace), ws_bytes, _stream(stream)), "pkv_prefill_varlen")
+        _raise(getattr(load(), entry)(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                      _ptr(block_tables), block_tables.shape[1], num_seqs, total_q, int(max_seqlen_q),
+                                      int(max_seqlen_k), hq, hkv, d, bs, nb, float(softmax_scale), _ptr(out),
+                                      _ptr(workspace), ws_bytes, _stream(stream)), entry)
     return out
+
+
+def pkv_prefill_varlen(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                       cu_seqlens_k: torch.Tensor, block_tables: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                       softmax_scale: float, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Varlen prefill attention over the paged cache (the new tokens' K/V already stored)."""
+    return _prefill("pkv_prefill_varlen", q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
+                    max_seqlen_q, max_seqlen_k, softmax_scale, out, workspace, stream)
+
+
+def pkv_prefill_plan(cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, total_q: int, max_seqlen_q: int,
+                     max_seqlen_k: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                     max_blocks_per_seq: int, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> torch.Tensor:
+    """Write the prefill work list for one batch into `workspace` (allocated if None) and return
+    it; every layer's pkv_prefill_varlen_planned call on this batch then reuses it."""
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _check(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    num_seqs = cu_seqlens_q.shape[0] - 1
+    if cu_seqlens_k.shape[0] != num_seqs + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k disagree on the sequence count")
+    if workspace is None:
+        n = pkv_prefill_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, int(max_seqlen_q))
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=cu_seqlens_q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with _on_device(cu_seqlens_q, cu_seqlens_k, workspace, stream=stream):
+        _raise(load().pkv_prefill_plan(_ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_blocks_per_seq), num_seqs,
+                                       int(total_q), int(max_seqlen_q), int(max_seqlen_k), int(num_heads),
+                                       int(num_kv_heads), int(head_dim), int(block_size), _ptr(workspace), ws_bytes,
+                                       _stream(stream)), "pkv_prefill_plan")
+    return workspace
+
+
+def pkv_prefill_varlen_planned(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               cu_seqlens_q: torch.Tensor, cu_seqlens_k: torch.Tensor, block_tables: torch.Tensor,
+                               max_seqlen_q: int, max_seqlen_k: int, softmax_scale: float, workspace: torch.Tensor,
+                               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pkv_prefill_varlen on the work list pkv_prefill_plan left in `workspace` (no planning launch)."""
+    return _prefill("pkv_prefill_varlen_planned", q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables,
+                    max_seqlen_q, max_seqlen_k, softmax_scale, out, workspace, stream)
 
 
 def pkv_decode_workspace_size(batch: int, num_heads: int, num_kv_heads: int, head_dim: int) -> int:

@@ -254,25 +254,31 @@ size_t pkv_prefill_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t n
     return prefill_workspace_bytes(num_seqs, max_seqlen_q, group_log2(num_heads, num_kv_heads));
 }
 
-pkv_status pkv_prefill_varlen(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
-                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                              const int32_t* block_tables, int32_t max_blocks_per_seq,
-                              int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
-                              int32_t max_seqlen_k, int32_t num_heads, int32_t num_kv_heads,
-                              int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                              float softmax_scale, pkv_bf16* out, void* workspace,
-                              size_t workspace_bytes, pkv_stream_t stream) {
-    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || max_blocks_per_seq <= 0 ||
-        num_blocks <= 0 || !(softmax_scale > 0.f) || softmax_scale == INFINITY)
+namespace {
+
+// Host checks and argument packing shared by the prefill entry points; q, k_cache,
+// v_cache and out are only checked when the call attends (not for a plan).
+pkv_status prefill_call(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* block_tables,
+                        int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                        int32_t max_seqlen_k, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t block_size, int32_t num_blocks, float softmax_scale, pkv_bf16* out,
+                        void* workspace, size_t workspace_bytes, pkv_stream_t stream, pkv::PrefillMode mode) {
+    const bool attends = mode != pkv::kPrefillPlanOnly;
+    if (num_seqs < 0 || total_q < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || max_blocks_per_seq <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (attends && (num_blocks <= 0 || !(softmax_scale > 0.f) || softmax_scale == INFINITY))
         return PKV_ERR_INVALID_ARG;
     if (!supported_shape(num_heads, num_kv_heads, head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
     if (max_seqlen_q > max_seqlen_k) return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
-    if (!q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k || !block_tables || !out)
-        return PKV_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
-         reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15)
-        return PKV_ERR_UNSUPPORTED;
+    if (!cu_seqlens_q || !cu_seqlens_k) return PKV_ERR_INVALID_ARG;
+    if (attends) {
+        if (!q || !k_cache || !v_cache || !block_tables || !out) return PKV_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+             reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15)
+            return PKV_ERR_UNSUPPORTED;
+    }
     if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
     int* err = device_error_word();
     if (!err) return PKV_ERR_CUDA;
@@ -296,7 +302,47 @@ pkv_status pkv_prefill_varlen(const pkv_bf16* q, const pkv_bf16* k_cache, const 
     a.softmax_scale = softmax_scale;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
-    return launch_prefill(a, err, as_stream(stream));
+    return launch_prefill(a, err, as_stream(stream), mode);
+}
+
+}  // namespace
+
+pkv_status pkv_prefill_varlen(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                              int32_t max_seqlen_k, int32_t num_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                              float softmax_scale, pkv_bf16* out, void* workspace,
+                              size_t workspace_bytes, pkv_stream_t stream) {
+    return prefill_call(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, max_blocks_per_seq,
+                        num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_dim,
+                        block_size, num_blocks, softmax_scale, out, workspace, workspace_bytes, stream,
+                        pkv::kPrefillPlanAndRun);
+}
+
+pkv_status pkv_prefill_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int32_t max_blocks_per_seq, int32_t num_seqs, int32_t total_q,
+                            int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size, void* workspace,
+                            size_t workspace_bytes, pkv_stream_t stream) {
+    return prefill_call(nullptr, nullptr, nullptr, cu_seqlens_q, cu_seqlens_k, nullptr, max_blocks_per_seq,
+                        num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_dim,
+                        block_size, 0, 0.f, nullptr, workspace, workspace_bytes, stream, pkv::kPrefillPlanOnly);
+}
+
+pkv_status pkv_prefill_varlen_planned(const pkv_bf16* q, const pkv_bf16* k_cache, const pkv_bf16* v_cache,
+                                      const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                                      int32_t max_seqlen_k, int32_t num_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                      float softmax_scale, pkv_bf16* out, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream) {
+    return prefill_call(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, max_blocks_per_seq,
+                        num_seqs, total_q, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads, head_dim,
+                        block_size, num_blocks, softmax_scale, out, workspace, workspace_bytes, stream,
+                        pkv::kPrefillRunOnly);
 }
 
 size_t pkv_decode_workspace_size(int32_t batch, int32_t num_heads, int32_t num_kv_heads,

@@ -119,7 +119,11 @@ struct PrefillArgs {
 
 // log_group = log2(num_heads / num_kv_heads)
 size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q, int log_group);
-pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream);
+// kPrefillPlanAndRun: plan the work list into the workspace, then attend;
+// kPrefillPlanOnly: the plan alone; kPrefillRunOnly: attend on the plan already
+// in the workspace (made for the same lengths, bounds and group size).
+enum PrefillMode { kPrefillPlanAndRun, kPrefillPlanOnly, kPrefillRunOnly };
+pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream, PrefillMode mode);
 
 // ---- a5 ---------------------------------------------------------------------
 cudaError_t launch_sample(const float* logits, int batch, int vocab, int64_t row_stride,

@@ -96,7 +96,7 @@ struct Params {
     const int32_t* cu_q;
     const int32_t* cu_k;
     const int32_t* block_tables;
-    const uint4* plan;        // [0].x = number of (seq, pair) records, [0].y = unit counter;
+    const uint4* plan;        // [0] = {number of (seq, pair) records, unit counter, 0, tag};
                               // then {seq << 16 | pair, q_start, q_len, k_len}, costliest first
     unsigned int* next_unit;  // &plan[0].y: units from gridDim.x on are taken in list order by atomic increments
     uint16_t* out;
@@ -107,6 +107,7 @@ struct Params {
     int block_size;
     int num_blocks;
     float scale_log2;
+    uint32_t tag;             // the plan this launch expects (see plan_tag)
     int* err;
 };
 
@@ -186,8 +187,13 @@ __device__ __forceinline__ Unit unit_from(const Params& p, int idx, uint4 rec) {
 // Next unit of the cost-sorted list for this CTA, or -1: CTA i starts with unit i,
 // and after that CTAs take units in list order as they free up (longest first,
 // so the last units to start are the shortest and the CTAs finish close together).
+// Every CTA that starts with a unit grabs until one grab fails, so one call makes exactly
+// `total` grabs; the last of them resets the counter, which leaves the plan ready for the
+// next call on it.  The reset sits in a CTA's last look-ahead, not at the kernel's end.
 __device__ __forceinline__ int grab_unit(const Params& p, int total) {
-    const int idx = static_cast<int>(atomicAdd(p.next_unit, 1u) + gridDim.x);
+    const unsigned int v = atomicAdd(p.next_unit, 1u);
+    if (v == static_cast<unsigned int>(total) - 1u) atomicExch(p.next_unit, 0u);
+    const int idx = static_cast<int>(v + gridDim.x);
     return idx < total ? idx : -1;
 }
 
@@ -216,17 +222,19 @@ __device__ __forceinline__ int unit_cost(int pr, int qtok, int ql, int off) {
 // -------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) prefill_plan_kernel(const int32_t* __restrict__ cu_q,
                                                            const int32_t* __restrict__ cu_k, int num_seqs,
-                                                           int max_blocks, int block_size, int qtok, int max_cost,
-                                                           uint4* __restrict__ plan, int* err) {
+                                                           int total_q, int max_blocks, int block_size, int qtok,
+                                                           int max_cost, uint32_t tag, uint4* __restrict__ plan,
+                                                           int* err) {
     extern __shared__ int hist[];          // [max_cost + 1]
     const int unit_tok = 2 * qtok;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int i = threadIdx.x; i <= max_cost; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     auto seq_ok = [&](int s, int& ql, int& kl) {
-        ql = cu_q[s + 1] - cu_q[s];
+        const int q0 = cu_q[s], q1 = cu_q[s + 1];
+        ql = q1 - q0;
         kl = cu_k[s + 1] - cu_k[s];
-        return ql >= 0 && ql <= kl && kl <= max_blocks * block_size;
+        return q0 >= 0 && q1 <= total_q && ql >= 0 && ql <= kl && kl <= max_blocks * block_size;
     };
     for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
         int ql, kl;
@@ -257,7 +265,7 @@ __global__ void __launch_bounds__(256) prefill_plan_kernel(const int32_t* __rest
             if (c >= 0) hist[c] = run + incl - x;
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) plan[0] = make_uint4(static_cast<uint32_t>(run), 0u, 0u, 0u);
+        if (lane == 0) plan[0] = make_uint4(static_cast<uint32_t>(run), 0u, 0u, tag);
     }
     __syncthreads();
     for (int s = threadIdx.x; s < num_seqs; s += blockDim.x) {
@@ -320,8 +328,11 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = misc[0];
     // everything above overlaps the plan kernel; global reads start here
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int total_units = static_cast<int>(*reinterpret_cast<const volatile unsigned int*>(p.plan)) *
-                            p.num_kv_heads;
+    // a plan made for other lengths, bounds or group size is not used: nothing is computed
+    const volatile unsigned int* head = reinterpret_cast<const volatile unsigned int*>(p.plan);
+    const bool plan_ok = head[3] == p.tag;
+    if (!plan_ok && blockIdx.x == 0 && tid == 0) record_error(p.err, PKV_DEVERR_PLAN, 0);
+    const int total_units = plan_ok ? static_cast<int>(head[0]) * p.num_kv_heads : 0;
 
     // Each warpgroup runs its own branch to the kernel's end (no common tail, so
     // every instruction has one register budget); every branch ends at the same
@@ -363,6 +374,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // first copies); the queue hands out the rest from unit gridDim.x on.
             int idx_cur = static_cast<int>(blockIdx.x) < total_units ? static_cast<int>(blockIdx.x) : -1;
             uint4 rec_cur = unit_record(p, idx_cur);
+            bool owe_grab = idx_cur >= 0;             // this CTA has yet to make its failing grab
             bool ok = true;
             if (idx_cur >= 0) {                       // group 0: the first unit's first K tile
                 k_at = locate(unit_from(p, idx_cur, rec_cur), 0);
@@ -379,6 +391,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mbar_arrive(bar(BAR_UF + slot));     // release: the entry is visible to the waiters
                 if (idx_cur < 0) break;
                 const int idx_nxt = grab_unit(p, total_units);  // its record is read for the last group
+                owe_grab = idx_nxt >= 0;
                 uint4 rec_nxt = make_uint4(0u, 0u, 0u, 0u);
                 bool rec_nxt_loaded = false;
                 const Unit u = unit_from(p, idx_cur, rec_cur);
@@ -433,6 +446,11 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 idx_cur = idx_nxt;
                 rec_cur = idx_nxt >= 0 ? rec_nxt : make_uint4(0u, 0u, 0u, 0u);
             }
+            // a CTA that stopped early takes what is left of the queue, so the call still makes its
+            // `total` grabs and the last of them resets the counter for the next call on the plan
+            if (owe_grab)
+                while (grab_unit(p, total_units) >= 0) {
+                }
             if (*ctl.abort) {
                 // copies already issued must land before shared memory is released
                 if (uq > 0) wait_drain(bar(BAR_QF), (uq - 1) & 1);
@@ -725,7 +743,17 @@ size_t prefill_workspace_bytes(int num_seqs, int max_seqlen_q, int log_group) {
     return align256((pairs + 1) * 16);
 }
 
-pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
+// The tag a plan carries: the launch arguments its records were built and checked against.
+static uint32_t plan_tag(const PrefillArgs& a, int lg, int max_cost) {
+    uint32_t h = 0x504b5650u;   // "PKVP"
+    const uint32_t f[6] = {static_cast<uint32_t>(a.num_seqs), static_cast<uint32_t>(a.total_q),
+                           static_cast<uint32_t>(lg), static_cast<uint32_t>(max_cost),
+                           static_cast<uint32_t>(a.max_blocks), static_cast<uint32_t>(a.block_size)};
+    for (uint32_t x : f) h = (h ^ x) * 0x01000193u;   // FNV-1a over the words
+    return h;
+}
+
+pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream, PrefillMode mode) {
     if (a.num_seqs == 0 || a.total_q == 0 || a.max_seqlen_q == 0) return PKV_OK;
     const int lg = group_log2(a.num_heads, a.num_kv_heads);
     if (lg < 0) return PKV_ERR_UNSUPPORTED;
@@ -733,6 +761,34 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     if (a.max_seqlen_q > 0xffff * unit_tok) return PKV_ERR_UNSUPPORTED;
     const size_t need = prefill_workspace_bytes(a.num_seqs, a.max_seqlen_q, lg);
     if (a.workspace == nullptr || a.workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a.workspace) & 15) return PKV_ERR_WORKSPACE;
+    const int max_cost = 2 * ((a.max_seqlen_k + KT - 1) / KT) + 1;   // unit_cost's largest value
+    const size_t plan_smem = static_cast<size_t>(max_cost + 1) * 4;
+    if (plan_smem > 200 * 1024) return PKV_ERR_UNSUPPORTED;
+    const uint32_t tag = plan_tag(a, lg, max_cost);
+
+    if (!setup_once(kSetupPrefill, [] {
+            return cudaFuncSetAttribute(prefill_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES) == cudaSuccess &&
+                   cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        200 * 1024) == cudaSuccess;
+        }))
+        return PKV_ERR_CUDA;
+    // the setmaxnreg split inside the kernel needs this many registers per thread at launch
+    static const int launch_regs = [] {
+        cudaFuncAttributes fa;
+        return cudaFuncGetAttributes(&fa, prefill_fa_kernel) == cudaSuccess ? fa.numRegs : -1;
+    }();
+    if (launch_regs < static_cast<int>(kMinLaunchRegs)) return PKV_ERR_UNSUPPORTED;
+
+    if (mode != kPrefillRunOnly) {
+        prefill_plan_kernel<<<1, 256, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.total_q, a.max_blocks,
+                                                            a.block_size, qtok, max_cost, tag,
+                                                            static_cast<uint4*>(a.workspace), err);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    if (mode == kPrefillPlanOnly) return PKV_OK;
+
     CUtensorMap tm_q, tm_k, tm_v;
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.num_heads),
@@ -756,9 +812,6 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
                          strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return PKV_ERR_INVALID_ARG;
     }
-    const int max_cost = 2 * ((a.max_seqlen_k + KT - 1) / KT) + 1;   // unit_cost's largest value
-    const size_t plan_smem = static_cast<size_t>(max_cost + 1) * 4;
-    if (plan_smem > 200 * 1024) return PKV_ERR_UNSUPPORTED;
     Params p;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
@@ -773,24 +826,8 @@ pkv_status launch_prefill(const PrefillArgs& a, int* err, cudaStream_t stream) {
     p.block_size = a.block_size;
     p.num_blocks = a.num_blocks;
     p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+    p.tag = tag;
     p.err = err;
-
-    if (!setup_once(kSetupPrefill, [] {
-            return cudaFuncSetAttribute(prefill_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES) == cudaSuccess &&
-                   cudaFuncSetAttribute(prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        200 * 1024) == cudaSuccess;
-        }))
-        return PKV_ERR_CUDA;
-    // the setmaxnreg split inside the kernel needs this many registers per thread at launch
-    static const int launch_regs = [] {
-        cudaFuncAttributes fa;
-        return cudaFuncGetAttributes(&fa, prefill_fa_kernel) == cudaSuccess ? fa.numRegs : -1;
-    }();
-    if (launch_regs < static_cast<int>(kMinLaunchRegs)) return PKV_ERR_UNSUPPORTED;
-    prefill_plan_kernel<<<1, 256, plan_smem, stream>>>(a.cu_q, a.cu_k, a.num_seqs, a.max_blocks, a.block_size,
-                                                        qtok, max_cost, static_cast<uint4*>(a.workspace), err);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
 
     const int64_t max_units = static_cast<int64_t>(a.num_seqs) *
                               ((a.max_seqlen_q + unit_tok - 1) / unit_tok) * a.num_kv_heads;

@@ -27,7 +27,8 @@ def declared_symbols():
 
 def test_header_declares_the_path():
     names = declared_symbols()
-    for must in ["pkv_slot_mapping", "pkv_store_kvcache", "pkv_prefill_varlen", "pkv_decode", "pkv_sample",
+    for must in ["pkv_slot_mapping", "pkv_store_kvcache", "pkv_prefill_varlen", "pkv_prefill_plan",
+                 "pkv_prefill_varlen_planned", "pkv_decode", "pkv_sample",
                  "pkv_decode_workspace_size", "pkv_get_device_error", "pkv_status_string"]:
         assert must in names
 
@@ -74,6 +75,14 @@ def test_host_argument_checks_return_before_launch(lib):
         assert lib.pkv_decode_append(P, P, P, P, P, P, 4, P, 2, 10, 16, 8, 128, 256, 4, bad, P, P, P, 0, P) == 1
     # prefill: max_seqlen_q > max_seqlen_k
     assert lib.pkv_prefill_varlen(P, P, P, P, P, P, 4, 2, 10, 9, 8, 16, 8, 128, 256, 4, 0.1, P, P, 0, P) == 1
+    # planned prefill: the plan checks the arguments it takes, the planned call those of pkv_prefill_varlen
+    assert lib.pkv_prefill_plan(P, P, 4, 2, 10, 9, 9, 16, 8, 128, 256, P, 0, P) == 1        # null cu_seqlens
+    assert lib.pkv_prefill_plan(P, P, 4, 2, 10, 9, 9, 12, 4, 128, 256, P, 0, P) == 2        # group of 3
+    assert lib.pkv_prefill_plan(P, P, 4, 2, 10, 9, 8, 16, 8, 128, 256, P, 0, P) == 1        # max_q > max_k
+    assert lib.pkv_prefill_plan(P, P, 4, 0, 10, 9, 9, 16, 8, 128, 256, P, 0, P) == 0        # no sequences
+    assert lib.pkv_prefill_varlen_planned(P, P, P, P, P, P, 4, 2, 10, 9, 9, 16, 8, 128, 256, 4, 0.1, P, P, 0, P) == 1
+    assert lib.pkv_prefill_varlen_planned(P, P, P, P, P, P, 4, 2, 10, 9, 9, 16, 8, 128, 256, 4, 0.0, P, P, 0, P) == 1
+    assert lib.pkv_prefill_varlen_planned(P, P, P, P, P, P, 4, 2, 10, 9, 9, 12, 4, 128, 256, 4, 0.1, P, P, 0, P) == 2
     # slot mapping: both or neither of cu_seqlens_k / context_lens
     assert lib.pkv_slot_mapping(P, P, P, P, 4, 2, 2, 256, 4, P, P) == 1
     # sample: row stride below vocab, empty vocab

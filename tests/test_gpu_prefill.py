@@ -117,3 +117,94 @@ def test_prefill_large_score_range_forces_rescale(pkv):
                             wl.block_tables, wl.block_size, wl.softmax_scale)
     assert_attention_close(out, ref, "large score range")
     expect_no_device_error(pkv)
+
+
+# ---- planned once per batch, run per layer -----------------------------------------------------
+
+def _plan(pkv, b, wl, hq, hkv, max_seqlen_k=None):
+    return pkv.pkv_prefill_plan(b.cu_q, b.cu_k, wl.total_q, int(wl.q_lens.max()),
+                                int(wl.kv_lens.max()) if max_seqlen_k is None else max_seqlen_k,
+                                hq, hkv, 128, wl.block_size, b.block_tables.shape[1])
+
+
+def test_prefill_plan_serves_every_layer(pkv):
+    """One plan, then three planned calls (three layers: their own q and pools, written in between
+    by the scatter) in order on one stream: each equals pkv_prefill_varlen on the same inputs bit for
+    bit and the oracle within tolerance; every call leaves the work queue reset for the next."""
+    wl = W.prefill_prefix()
+    layers = [GpuBatch(wl, W.paged_values(wl, layer=i)) for i in range(3)]
+    hq, hkv = layers[0].q.shape[1], layers[0].k_cache.shape[2]
+    ws = _plan(pkv, layers[0], wl, hq, hkv)
+    outs = []
+    for b in layers:
+        b.run_slots_and_store(pkv, decode=False)
+        outs.append(pkv.pkv_prefill_varlen_planned(b.q, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables,
+                                                   int(wl.q_lens.max()), int(wl.kv_lens.max()),
+                                                   wl.softmax_scale, ws))
+    for i, b in enumerate(layers):
+        ref = b.run_prefill(pkv)
+        assert torch.equal(outs[i].view(torch.int16), ref.view(torch.int16)), f"layer {i}"
+    assert_attention_close(outs[2], layers[2].oracle_prefill(), "third planned layer")
+    expect_no_device_error(pkv)
+
+
+def test_prefill_planned_call_on_a_plan_for_other_arguments(pkv):
+    """A plan made for another max_seqlen_k (so other cost buckets) is not used: the planned call
+    computes nothing, leaves out as it was and records the plan error."""
+    wl = W.prefill_prefix()
+    b = GpuBatch(wl, W.paged_values(wl))
+    b.run_slots_and_store(pkv, decode=False)
+    hq, hkv = b.q.shape[1], b.k_cache.shape[2]
+    ws = _plan(pkv, b, wl, hq, hkv, max_seqlen_k=int(wl.kv_lens.max()) + 1024)
+    out = torch.full_like(b.q, 7.0)
+    pkv.pkv_prefill_varlen_planned(b.q, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables,
+                                   int(wl.q_lens.max()), int(wl.kv_lens.max()), wl.softmax_scale, ws, out=out)
+    code, _ = pkv.pkv_get_device_error(clear=True)
+    assert code == 7
+    assert bool((out == 7.0).all())
+    # the same workspace, planned again for the right arguments, works
+    pkv.pkv_prefill_plan(b.cu_q, b.cu_k, wl.total_q, int(wl.q_lens.max()), int(wl.kv_lens.max()), hq, hkv, 128,
+                         wl.block_size, b.block_tables.shape[1], workspace=ws)
+    pkv.pkv_prefill_varlen_planned(b.q, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables,
+                                   int(wl.q_lens.max()), int(wl.kv_lens.max()), wl.softmax_scale, ws, out=out)
+    assert_attention_close(out, b.oracle_prefill(), "after planning again")
+    expect_no_device_error(pkv)
+
+
+def test_prefill_plan_and_planned_calls_in_a_cuda_graph(pkv):
+    """plan + two planned layers captured once; replays with new q in the captured buffer match
+    eager pkv_prefill_varlen bit for bit."""
+    wl = W.prefill_prefix()
+    b = GpuBatch(wl, W.paged_values(wl))
+    b.run_slots_and_store(pkv, decode=False)
+    hq, hkv = b.q.shape[1], b.k_cache.shape[2]
+    ws = torch.empty(pkv.pkv_prefill_workspace_size(len(wl.q_lens), hq, hkv, 128, int(wl.q_lens.max())),
+                     dtype=torch.uint8, device="cuda")
+    o1, o2 = torch.empty_like(b.q), torch.empty_like(b.q)
+    q2 = b.q.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    args = (int(wl.q_lens.max()), int(wl.kv_lens.max()), wl.softmax_scale, ws)
+    with torch.cuda.stream(s):
+        def step():
+            pkv.pkv_prefill_plan(b.cu_q, b.cu_k, wl.total_q, int(wl.q_lens.max()), int(wl.kv_lens.max()), hq, hkv,
+                                 128, wl.block_size, b.block_tables.shape[1], workspace=ws)
+            pkv.pkv_prefill_varlen_planned(b.q, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables, *args, out=o1)
+            pkv.pkv_prefill_varlen_planned(q2, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables, *args, out=o2)
+        step()                      # warm-up outside the capture
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    gen = torch.Generator().manual_seed(5)
+    for _ in range(2):
+        b.q.copy_(torch.randn(b.q.shape, generator=gen).to(torch.bfloat16))
+        q2.copy_(torch.randn(q2.shape, generator=gen).to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        r1 = b.run_prefill(pkv)
+        r2 = pkv.pkv_prefill_varlen(q2, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables,
+                                    int(wl.q_lens.max()), int(wl.kv_lens.max()), wl.softmax_scale)
+        assert torch.equal(o1.view(torch.int16), r1.view(torch.int16))
+        assert torch.equal(o2.view(torch.int16), r2.view(torch.int16))
+    expect_no_device_error(pkv)
