@@ -328,11 +328,6 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = misc[0];
     // everything above overlaps the plan kernel; global reads start here
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // a plan made for other lengths, bounds or group size is not used: nothing is computed
-    const volatile unsigned int* head = reinterpret_cast<const volatile unsigned int*>(p.plan);
-    const bool plan_ok = head[3] == p.tag;
-    if (!plan_ok && blockIdx.x == 0 && tid == 0) record_error(p.err, PKV_DEVERR_PLAN, 0);
-    const int total_units = plan_ok ? static_cast<int>(head[0]) * p.num_kv_heads : 0;
 
     // Each warpgroup runs its own branch to the kernel's end (no common tail, so
     // every instruction has one register budget); every branch ends at the same
@@ -341,6 +336,14 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         regs_dec<kControlRegs>();
         // ---------------------------------------------------------------- TMA
         if (lane == 0) {
+            // The plan's header and this CTA's first record, read together (one round trip; the
+            // record of unit blockIdx.x lies inside the workspace whatever the header says).  A
+            // plan made for other lengths, bounds or group size is not used: nothing is computed.
+            const uint4 head = __ldcg(p.plan);
+            const uint4 rec_first = __ldcg(p.plan + 1 + blockIdx.x / p.num_kv_heads);
+            const bool plan_ok = head.w == p.tag;
+            if (!plan_ok && blockIdx.x == 0) record_error(p.err, PKV_DEVERR_PLAN, 0);
+            const int total_units = plan_ok ? static_cast<int>(head.x) * p.num_kv_heads : 0;
             int uq = 0, groups = 0;   // Q tiles and K/V groups issued
             // a tile's K or V: TMA from the physical block the table names (128 keys, two 64-dim halves)
             // where tile jj of unit w lives: its physical block (from the block table) and the offset
@@ -373,7 +376,7 @@ prefill_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // has not started.  The first unit of CTA i is unit i (no atomic round trip before the
             // first copies); the queue hands out the rest from unit gridDim.x on.
             int idx_cur = static_cast<int>(blockIdx.x) < total_units ? static_cast<int>(blockIdx.x) : -1;
-            uint4 rec_cur = unit_record(p, idx_cur);
+            uint4 rec_cur = idx_cur >= 0 ? rec_first : make_uint4(0u, 0u, 0u, 0u);
             bool owe_grab = idx_cur >= 0;             // this CTA has yet to make its failing grab
             bool ok = true;
             if (idx_cur >= 0) {                       // group 0: the first unit's first K tile
