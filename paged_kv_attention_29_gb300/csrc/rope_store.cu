@@ -124,6 +124,10 @@ constexpr int kStoresInFlight = 3;      // store groups still reading their stag
 constexpr int kRotWarps = 4;
 constexpr int kStagedThreads = 32 * (kRotWarps + 2);
 constexpr int kMaxStageBytes = 16384;
+// The loader refills a stage only after the store warp releases it, which happens kStoresInFlight
+// tokens after that stage's token; with no more stages than that, the loader and the store warp
+// would wait on each other.
+static_assert(kStages > kStoresInFlight, "the stage ring must be deeper than the stores in flight");
 
 __global__ void __launch_bounds__(kStagedThreads) rope_store_staged_kernel(RopeStoreArgs a, int64_t n_tokens,
                                                                            int* err) {
