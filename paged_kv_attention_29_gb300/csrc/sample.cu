@@ -170,16 +170,17 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
         const int q1 = min(nquads, q0 + per);
         // Pruning.  With t = best - l/T, an element can beat `best` only if
         // -ln(-ln u) > t, i.e. -ln u < e^-t; since -ln u >= 1 - u that needs
-        // 1 - u < e^-t.  And -ln(-ln u) <= 16.64 for every u the generator makes
-        // (u <= 1 - 2^-24), so a quad whose largest l/T + 16.7 is below `best` has
-        // no candidate at all and skips its Philox call.  `best` is the warp's
-        // running maximum; t carries a 1e-3 margin and the bound a factor 1.001,
-        // so rounding and exact ties are always decided by the exact key.  A quad
-        // that does draw noise is first tested as a whole: its smallest 1 - u (its
-        // largest word) against the bound of its largest logit.  Any candidate
-        // passes that test, and only a passing quad tests its elements one by one
-        // and takes the exact key of each candidate.  Skipped elements cannot
-        // change the winner: some element of the warp already has a larger key.
+        // 1 - u < e^-t.  `best` is the warp's running maximum; t carries a 1e-3
+        // margin and the bound a factor 1.001, so rounding and exact ties are
+        // always decided by the exact key.  Every quad draws its noise (a test of
+        // its largest logit against `best` before the Philox call -- no candidate
+        // is possible when l/T + 16.7 < best, since -ln(-ln u) <= 16.64 for every
+        // u the generator makes -- skips only about 6% of the calls here and cost
+        // more than it saved).  A quad is first tested as a whole: its smallest
+        // 1 - u (its largest word) against the bound of its largest logit.  Any
+        // candidate passes that test, and only a passing quad tests its elements
+        // one by one and takes the exact key of each candidate.  Skipped elements
+        // cannot change the winner: some element of the warp already has a larger key.
         const int iters = (q1 - q0 + THREADS - 1) / THREADS;     // uniform across the CTA
         float wbest = -INFINITY;
         // the next quad's logits are loaded one iteration ahead, so the load is in flight while
@@ -198,21 +199,18 @@ sample_race_kernel(const float* __restrict__ logits, int vocab, int64_t row_stri
             const int col = qd * 4;
             const float best = wbest;     // the warp's best after the previous quad, so never below bk
             const float lmax = fmax3(l[0], l[1], fmaxf(l[2], l[3]));
-            // (NaN logits fail this test; their bound below is NaN, so they are never candidates)
-            if (!(lmax * inv_t + 16.7f < best)) {
-                const uint4 x = philox_row_at<kParamKeys>(static_cast<uint32_t>(qd), prow, rk);
-                // candidate test: 1 - u < 1.001 e^-t, t = best - l/T - 1e-3, as 1 - u < 2^(l (log2 e / T) + cb).
-                // t <= 0 gives a bound above 1 (always a candidate); l = -inf (padding past the
-                // vocabulary) gives 0 (never); NaN never.
-                const float cb = (1e-3f - best) * 1.4426950408889634f + 1.4419741739064e-3f;   // + log2 1.001
-                const uint32_t xmax = max(max(x.x, x.y), max(x.z, x.w));
-                if (one_minus_u_of(xmax) < ex2_ftz(fmaf(lmax, inv_t_log2e, cb))) {
-                    const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+            const uint4 x = philox_row_at<kParamKeys>(static_cast<uint32_t>(qd), prow, rk);
+            // candidate test: 1 - u < 1.001 e^-t, t = best - l/T - 1e-3, as 1 - u < 2^(l (log2 e / T) + cb).
+            // t <= 0 gives a bound above 1 (always a candidate); l = -inf (padding past the
+            // vocabulary) gives 0 (never); NaN never.
+            const float cb = (1e-3f - best) * 1.4426950408889634f + 1.4419741739064e-3f;   // + log2 1.001
+            const uint32_t xmax = max(max(x.x, x.y), max(x.z, x.w));
+            if (one_minus_u_of(xmax) < ex2_ftz(fmaf(lmax, inv_t_log2e, cb))) {
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (one_minus_u_of(xs[e]) < ex2_ftz(fmaf(l[e], inv_t_log2e, cb)))
-                            consider(l[e], inv_t, xs[e], col + e, bk, bi);
-                }
+                for (int e = 0; e < 4; ++e)
+                    if (one_minus_u_of(xs[e]) < ex2_ftz(fmaf(l[e], inv_t_log2e, cb)))
+                        consider(l[e], inv_t, xs[e], col + e, bk, bi);
             }
         };
         // iterations in which every thread's quad exists and is four aligned columns: no checks
