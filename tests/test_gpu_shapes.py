@@ -40,6 +40,13 @@ def test_prefill_other_shapes(pkv, shape):
     assert np.array_equal(b.slots.cpu().numpy().astype(np.int64), b.oracle_slots())
     out = b.run_prefill(pkv)
     assert_attention_close(out, b.oracle_prefill(), f"prefill {shape}")
+    # the same attention on a plan made once (its tag covers the group size and block size)
+    hq, hkv, d = b.q.shape[1], b.k_cache.shape[2], b.q.shape[2]
+    mq, mk = int(wl.q_lens.max()), int(wl.kv_lens.max())
+    ws = pkv.pkv_prefill_plan(b.cu_q, b.cu_k, wl.total_q, mq, mk, hq, hkv, d, wl.block_size, b.block_tables.shape[1])
+    planned = pkv.pkv_prefill_varlen_planned(b.q, b.k_cache, b.v_cache, b.cu_q, b.cu_k, b.block_tables, mq, mk,
+                                             wl.softmax_scale, ws)
+    assert torch.equal(planned.view(torch.int16), out.view(torch.int16)), f"planned prefill {shape}"
     expect_no_device_error(pkv)
 
 
