@@ -208,3 +208,36 @@ def test_prefill_plan_and_planned_calls_in_a_cuda_graph(pkv):
         assert torch.equal(o1.view(torch.int16), r1.view(torch.int16))
         assert torch.equal(o2.view(torch.int16), r2.view(torch.int16))
     expect_no_device_error(pkv)
+
+
+def test_prefill_plan_lists_every_unit_costliest_first(pkv):
+    """The plan's records, read back from the workspace: exactly one record per (sequence, pair of
+    128/G-token tiles) with its query start and lengths, the header's count equal to their number,
+    and the list ordered by non-increasing cost (twice the longer tile's KV tiles, plus one when
+    the second tile has tokens).  Ties may come in any order."""
+    wl = W.prefill_prefix()
+    b = GpuBatch(wl, W.paged_values(wl))
+    hq, hkv = b.q.shape[1], b.k_cache.shape[2]
+    ws = _plan(pkv, b, wl, hq, hkv)
+    torch.cuda.synchronize()
+    words = ws.view(torch.int32).cpu().numpy()
+    qtok = 128 // (hq // hkv)
+    expect = []
+    for s, (ql, kl) in enumerate(zip(wl.q_lens.astype(int), wl.kv_lens.astype(int))):
+        for pr in range(-(-ql // (2 * qtok))):
+            expect.append((s, pr, int(wl.cu_seqlens_q[s]), ql, kl))
+    n = int(words[0])
+    assert n == len(expect)
+    recs = words[4:4 + 4 * n].reshape(n, 4)
+    got = sorted((int(r[0]) >> 16, int(r[0]) & 0xFFFF, int(r[1]), int(r[2]), int(r[3])) for r in recs)
+    assert got == sorted(expect)
+
+    def tiles(first, ql, off):
+        return 0 if first >= ql else (min(first + qtok, ql) - 1 + off + 128) // 128
+
+    costs = []
+    for r in recs:
+        pr, ql, kl = int(r[0]) & 0xFFFF, int(r[2]), int(r[3])
+        na, nb = tiles(pr * 2 * qtok, ql, kl - ql), tiles(pr * 2 * qtok + qtok, ql, kl - ql)
+        costs.append(2 * max(na, nb) + (1 if nb > 0 else 0))
+    assert all(costs[i] >= costs[i + 1] for i in range(n - 1))
